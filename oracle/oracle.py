@@ -1,0 +1,271 @@
+"""numpy-level API over the C oracle (``fp4q_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY (tests, smoke check, CPU-baseline leg of the benchmark).
+
+bf16 tensors are passed as ``np.uint16`` bit patterns. Packed NVFP4 codes are
+``[rows, cols/2]`` bytes with element ``2j`` in the low nibble; NVFP4 scales are
+E4M3 bytes, ``[rows, cols/16]`` (1D) or ``[rows/16, cols/16]`` (16x16 tiles);
+MXFP8 is E4M3 bytes ``[rows, cols]`` plus E8M0 bytes ``[rows, cols/32]``.
+
+The GEMM references dequantize each operand exactly (in float64) and multiply with
+a float64 matmul: the block-scaled GEMM of the pages ("Pretraining Large Language
+Models with NVFP4", Quantization Procedure step 5; 4bit.vizuara.ai §7) is, up to the
+order of its fp32 additions, exactly this product.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_u32p = ctypes.POINTER(ctypes.c_uint32)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
+_i64 = ctypes.c_int64
+
+RNE, SR = 0, 1
+IN_BF16, IN_NVFP4_1D, IN_NVFP4_2D = 0, 1, 2
+
+
+def lib():
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        L.orc_e2m1_decode.restype = ctypes.c_double
+        L.orc_e2m1_decode.argtypes = [ctypes.c_uint32]
+        L.orc_e2m1_encode_rne.restype = ctypes.c_uint32
+        L.orc_e2m1_encode_rne.argtypes = [ctypes.c_float]
+        L.orc_e2m1_encode_sr.restype = ctypes.c_uint32
+        L.orc_e2m1_encode_sr.argtypes = [ctypes.c_float, ctypes.c_uint32]
+        L.orc_e4m3_decode.restype = ctypes.c_double
+        L.orc_e4m3_decode.argtypes = [ctypes.c_uint32]
+        L.orc_e4m3_encode_rne_sat.restype = ctypes.c_uint32
+        L.orc_e4m3_encode_rne_sat.argtypes = [ctypes.c_float]
+        L.orc_e4m3_encode_sr.restype = ctypes.c_uint32
+        L.orc_e4m3_encode_sr.argtypes = [ctypes.c_float, ctypes.c_uint32]
+        L.orc_pow2_ceil_exponent.restype = ctypes.c_int
+        L.orc_pow2_ceil_exponent.argtypes = [ctypes.c_double, ctypes.c_double]
+        L.orc_philox4x32_10.restype = None
+        L.orc_philox4x32_10.argtypes = [_u32p, _u32p, _u32p]
+        L.orc_sr_bits16.restype = ctypes.c_uint32
+        L.orc_sr_bits16.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint64]
+        L.orc_amax_bf16.restype = ctypes.c_float
+        L.orc_amax_bf16.argtypes = [_u16p, _i64, _i64, _i64]
+        L.orc_global_scales.restype = None
+        L.orc_global_scales.argtypes = [ctypes.c_float, _f32p, _f32p]
+        L.orc_block_scale_code.restype = ctypes.c_uint32
+        L.orc_block_scale_code.argtypes = [ctypes.c_float, ctypes.c_float]
+        L.orc_block_encode_scale.restype = ctypes.c_float
+        L.orc_block_encode_scale.argtypes = [ctypes.c_uint32, ctypes.c_float]
+        for fn in (L.orc_quantize_1d, L.orc_quantize_2d):
+            fn.restype = None
+            fn.argtypes = [_u16p, _i64, _i64, _i64, _f32p, _u8p, _u8p, _f32p, _f32p]
+        L.orc_dequant_nvfp4.restype = None
+        L.orc_dequant_nvfp4.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_float, _i64, _i64,
+                                        _f32p, _f64p]
+        L.orc_dequant_mxfp8.restype = None
+        L.orc_dequant_mxfp8.argtypes = [_u8p, _u8p, _i64, _i64, _f64p]
+        L.orc_rht16_group.restype = None
+        L.orc_rht16_group.argtypes = [_f32p, ctypes.c_uint32]
+        L.orc_rht16.restype = None
+        L.orc_rht16.argtypes = [ctypes.c_void_p, ctypes.c_int, _f32p, _i64, _i64, ctypes.c_uint32]
+        L.orc_mxfp8_block.restype = None
+        L.orc_mxfp8_block.argtypes = [_f32p, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32,
+                                      ctypes.c_uint64, _u8p, _u8p]
+        L.orc_requant_mxfp8.restype = None
+        L.orc_requant_mxfp8.argtypes = [ctypes.c_int, ctypes.c_void_p, _u8p, ctypes.c_float,
+                                        _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
+                                        ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32, _u8p, _u8p]
+        _LIB = L
+    return _LIB
+
+
+def _p(a, t):
+    return a.ctypes.data_as(t)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---------------------------------------------------------------- formats
+def e2m1_decode(code):
+    return lib().orc_e2m1_decode(int(code))
+
+
+def e2m1_encode_rne(v):
+    return lib().orc_e2m1_encode_rne(float(v))
+
+
+def e2m1_encode_sr(v, r16):
+    return lib().orc_e2m1_encode_sr(float(v), int(r16))
+
+
+def e4m3_decode(code):
+    return lib().orc_e4m3_decode(int(code))
+
+
+def e4m3_encode_rne_sat(v):
+    return lib().orc_e4m3_encode_rne_sat(float(v))
+
+
+def e4m3_encode_sr(v, r16):
+    return lib().orc_e4m3_encode_sr(float(v), int(r16))
+
+
+def pow2_ceil_exponent(amax, vmax):
+    return lib().orc_pow2_ceil_exponent(float(amax), float(vmax))
+
+
+def philox4x32_10(ctr, key):
+    c = _c(ctr, np.uint32)
+    k = _c(key, np.uint32)
+    out = np.zeros(4, np.uint32)
+    lib().orc_philox4x32_10(_p(c, _u32p), _p(k, _u32p), _p(out, _u32p))
+    return out
+
+
+def sr_bits16(seed, tag, idx):
+    return lib().orc_sr_bits16(int(seed), int(tag), int(idx))
+
+
+def global_scales(amax):
+    e = ctypes.c_float()
+    d = ctypes.c_float()
+    lib().orc_global_scales(float(amax), ctypes.byref(e), ctypes.byref(d))
+    return e.value, d.value
+
+
+def block_scale_code(amax_b, s_enc):
+    return lib().orc_block_scale_code(float(amax_b), float(s_enc))
+
+
+def block_encode_scale(sb, s_dec):
+    return lib().orc_block_encode_scale(int(sb), float(s_dec))
+
+
+# ---------------------------------------------------------------- tensors
+def amax_bf16(x):
+    x = _c(x, np.uint16)
+    return lib().orc_amax_bf16(_p(x, _u16p), x.shape[0], x.shape[1], x.shape[1])
+
+
+def _quantize(fn, x, amax, tile):
+    x = _c(x, np.uint16)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    scales = np.zeros((rows // 16, cols // 16) if tile else (rows, cols // 16), np.uint8)
+    a_in = None if amax is None else ctypes.byref(ctypes.c_float(amax))
+    a_out = ctypes.c_float()
+    s_dec = ctypes.c_float()
+    fn(_p(x, _u16p), rows, cols, cols, a_in, _p(codes, _u8p), _p(scales, _u8p),
+       ctypes.byref(a_out), ctypes.byref(s_dec))
+    return codes, scales, a_out.value, s_dec.value
+
+
+def quantize_1d(x, amax=None):
+    """NVFP4 with 1x16 blocks along rows -> (codes, scales, amax, s_dec)."""
+    return _quantize(lib().orc_quantize_1d, x, amax, tile=False)
+
+
+def quantize_2d(w, amax=None):
+    """NVFP4 with 16x16 tile scales -> (codes, tile_scales, amax, s_dec)."""
+    return _quantize(lib().orc_quantize_2d, w, amax, tile=True)
+
+
+def dequant_nvfp4(codes, scales, scale_kind, s_dec, as_f32=False):
+    """scale_kind 1 = 1D [rows, cols/16], 2 = tiles [rows/16, cols/16]."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    rows, cols = codes.shape[0], codes.shape[1] * 2
+    if as_f32:
+        out = np.zeros((rows, cols), np.float32)
+        lib().orc_dequant_nvfp4(_p(codes, _u8p), _p(scales, _u8p), scale_kind, float(s_dec),
+                                rows, cols, _p(out, _f32p), None)
+    else:
+        out = np.zeros((rows, cols), np.float64)
+        lib().orc_dequant_nvfp4(_p(codes, _u8p), _p(scales, _u8p), scale_kind, float(s_dec),
+                                rows, cols, None, _p(out, _f64p))
+    return out
+
+
+def dequant_mxfp8(e4m3, e8m0):
+    e4m3 = _c(e4m3, np.uint8)
+    e8m0 = _c(e8m0, np.uint8)
+    rows, cols = e4m3.shape
+    out = np.zeros((rows, cols), np.float64)
+    lib().orc_dequant_mxfp8(_p(e4m3, _u8p), _p(e8m0, _u8p), rows, cols, _p(out, _f64p))
+    return out
+
+
+def rht16_group(v, signs):
+    v = _c(v, np.float32).copy()
+    lib().orc_rht16_group(_p(v, _f32p), int(signs))
+    return v
+
+
+def rht16(x, signs, is_bf16=False):
+    x = _c(x, np.uint16 if is_bf16 else np.float32)
+    rows, cols = x.shape
+    out = np.zeros((rows, cols), np.float32)
+    lib().orc_rht16(x.ctypes.data, int(bool(is_bf16)), _p(out, _f32p), rows, cols, int(signs))
+    return out
+
+
+def mxfp8_block(v, rounding=RNE, seed=0, tag=0, out_idx0=0):
+    v = _c(v, np.float32)
+    e4 = np.zeros(32, np.uint8)
+    e8 = np.zeros(1, np.uint8)
+    lib().orc_mxfp8_block(_p(v, _f32p), rounding, int(seed), int(tag), int(out_idx0),
+                          _p(e4, _u8p), _p(e8, _u8p))
+    return e4, int(e8[0])
+
+
+def requant_mxfp8(in_kind, data, scales, s_dec, rows, cols, transpose, rht, rht_signs,
+                  rounding, seed, tag):
+    """Dequantize -> [transpose] -> [RHT16] -> MXFP8 -> (e4m3, e8m0)."""
+    if in_kind == IN_BF16:
+        data = _c(data, np.uint16)
+        sc = None
+    else:
+        data = _c(data, np.uint8)
+        scales = _c(scales, np.uint8)
+        sc = _p(scales, _u8p)
+    orows, ocols = (cols, rows) if transpose else (rows, cols)
+    e4 = np.zeros((orows, ocols), np.uint8)
+    e8 = np.zeros((orows, ocols // 32), np.uint8)
+    lib().orc_requant_mxfp8(in_kind, data.ctypes.data, sc, float(s_dec), rows, cols,
+                            int(bool(transpose)), int(bool(rht)), int(rht_signs), rounding,
+                            int(seed), int(tag), _p(e4, _u8p), _p(e8, _u8p))
+    return e4, e8
+
+
+# ---------------------------------------------------------------- GEMMs
+def gemm_nvfp4(a_codes, a_scales, a_kind, a_sdec, b_codes, b_scales, b_kind, b_sdec):
+    """D = A . B^T on exactly dequantized NVFP4 operands, float64."""
+    A = dequant_nvfp4(a_codes, a_scales, a_kind, a_sdec)
+    B = dequant_nvfp4(b_codes, b_scales, b_kind, b_sdec)
+    return A @ B.T
+
+
+def gemm_mxfp8(a_e4m3, a_e8m0, b_e4m3, b_e8m0):
+    """D = A . B^T on exactly dequantized MXFP8 operands, float64."""
+    return dequant_mxfp8(a_e4m3, a_e8m0) @ dequant_mxfp8(b_e4m3, b_e8m0).T
+
+
+def round_bf16(x):
+    """float -> nearest-even bf16, returned as float32 values."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint32) << 16
+    return r.astype(np.uint32).view(np.float32)
+
+
+__all__ = [n for n in dir() if not n.startswith("_") and n not in ("ctypes", "os", "np", "lib")]
+__all__ += ["lib"]
