@@ -1,0 +1,208 @@
+/*
+ * fp4q.h — C ABI of libfp4q.so: the hot path of the NVFP4 linear layer on one GB300.
+ *
+ * Forward: NVFP4 quantize of activations (1x16 blocks) and weights (16x16 tiles), then a
+ * block-scaled NVFP4 x NVFP4 GEMM with FP32 accumulation. Backward: dequantize, transpose
+ * and re-quantize to MXFP8 with stochastic rounding, an optional 16-point random Hadamard
+ * transform on the wgrad operands, then MXFP8 dgrad / wgrad GEMMs.
+ *
+ * Sources (web pages, by title and section):
+ *   [NV]  "Pretraining Large Language Models with NVFP4" (arXiv 2509.25149), summary page:
+ *         "NVFP4 Format and Quantization Procedure" steps 1-5; "Random Hadamard Transforms";
+ *         "Two-Dimensional Weight Scaling and the Chain Rule Problem";
+ *         "Stochastic Rounding for Unbiased Gradients".
+ *   [VZ]  "End-to-End 4-Bit Training" rebuilt on one B200 (4bit.vizuara.ai), §5-§13.
+ *   [TML] "End-to-End 4-Bit Training" (Thinking Machines), "基于随机舍入的重量化".
+ *   [AC]  "FP4 Training on Blackwell" (aicassindra.com), "The scaling math, worked".
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are row-major. bf16 inputs are 16-bit IEEE bfloat16.
+ *   - Pointers are device pointers unless stated otherwise. The caller owns and allocates
+ *     every buffer, including the small workspaces; the library allocates nothing and keeps
+ *     no state between calls other than a device-side error word (fp4q_device_status).
+ *   - Work is enqueued asynchronously on `stream` (NULL = the legacy default stream). Scalars
+ *     (amax, s_dec) stay on the device; no call synchronizes the host.
+ *   - Arguments are validated on the host before any launch. A failed check returns a
+ *     status and launches nothing. A launch error maps to FP4Q_ERR_CUDA.
+ *   - Packed NVFP4 codes: E2M1, two per byte, element 2j in the low nibble, 2j+1 in the high
+ *     nibble; a row of `cols` values takes cols/2 bytes. NVFP4 block scales: one E4M3 byte
+ *     per block, row-major. MXFP8: one E4M3 byte per value plus one E8M0 byte per 32
+ *     consecutive values of a row (value = e4m3 * 2^(e8m0 - 127)).
+ *   - Non-finite inputs (inf, NaN) are outside the method; their outputs are unspecified.
+ */
+#ifndef FP4Q_H
+#define FP4Q_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FP4Q_API __attribute__((visibility("default")))
+#else
+#define FP4Q_API
+#endif
+
+/* A CUDA stream handle (the same object as cudaStream_t). */
+typedef struct CUstream_st* fp4q_stream_t;
+
+enum fp4q_status {
+    FP4Q_OK = 0,
+    FP4Q_ERR_NULL = 1,        /* a required pointer is NULL                               */
+    FP4Q_ERR_ALIGN = 2,       /* a pointer or leading dimension breaks the 16-byte rule    */
+    FP4Q_ERR_SHAPE = 3,       /* a size is zero, negative or not a required multiple       */
+    FP4Q_ERR_ARG = 4,         /* an enum or flag argument is out of range                  */
+    FP4Q_ERR_CUDA = 5,        /* a CUDA launch or runtime call failed                      */
+    FP4Q_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up (fp4q_device_status)  */
+    FP4Q_ERR_UNSUPPORTED = 7  /* the current device is not sm_103 / sm_100 class          */
+};
+
+enum fp4q_in_kind { FP4Q_IN_BF16 = 0, FP4Q_IN_NVFP4_1D = 1, FP4Q_IN_NVFP4_2D = 2 };
+enum fp4q_rounding { FP4Q_RNE = 0, FP4Q_SR = 1 };
+enum fp4q_dtype { FP4Q_F32 = 0, FP4Q_BF16 = 1 };
+enum fp4q_scale_kind { FP4Q_SCALE_1D = 1, FP4Q_SCALE_2D = 2 };
+
+/* Human-readable name of a status code (static string, never NULL). */
+FP4Q_API const char* fp4q_status_str(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+FP4Q_API int fp4q_version(void);
+
+/*
+ * fp4q_quantize_1d — NVFP4 quantize with 1x16 blocks along each row.
+ * [NV] "NVFP4 Format and Quantization Procedure", steps 1-4; [VZ] §5-6.
+ *   amax   = max |x| over the tensor                      (step 1; the extra HBM pass)
+ *   s_enc  = 2688 / amax (fp32), s_dec = 1 / s_enc;  amax == 0 -> s_enc = s_dec = 1
+ *   per block b of 16: sb = E4M3_RNE((amax_b / 6) * s_enc), raised to 0x01 if it is 0
+ *                      s_enc_b = 1 / (fp32(sb) * s_dec)
+ *                      code_i = E2M1_RNE(x_i * s_enc_b)    (ties to even, saturating)
+ *   x_bf16    [rows][ld] bf16, 16-byte aligned, ld % 8 == 0, ld >= cols
+ *   amax_in   device float or NULL. If given, it is used as the tensor amax (for example an
+ *             amax agreed across shards) and amax_ws may be NULL.
+ *   amax_ws   device float workspace (4 bytes) that receives the computed amax; required when
+ *             amax_in is NULL. It is overwritten.
+ *   codes     [rows][cols/2] bytes, 16-byte aligned; scales [rows][cols/16] E4M3 bytes
+ *   s_dec_out device float: the per-tensor decode scale s_dec.
+ *   rows >= 1, cols >= 16, cols % 16 == 0.
+ */
+FP4Q_API int fp4q_quantize_1d(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld,
+                     const float* amax_in, float* amax_ws,
+                     uint8_t* codes, uint8_t* scales, float* s_dec_out, fp4q_stream_t stream);
+
+/*
+ * fp4q_quantize_2d — NVFP4 quantize of a weight with one E4M3 scale per 16x16 tile, so the
+ * row-wise and column-wise views share scales. [NV] "Two-Dimensional Weight Scaling and the
+ * Chain Rule Problem"; [VZ] §8. Same arithmetic as fp4q_quantize_1d with amax_b taken over
+ * the 256 values of a tile. `batch` independent tensors (e.g. MoE experts), each with its
+ * own amax and s_dec, sit `batch_stride` elements apart.
+ *   w_bf16      [batch][rows][ld] bf16, 16-byte aligned, ld % 8 == 0, batch_stride % 8 == 0
+ *   amax_in     device float[batch] or NULL; amax_ws device float[batch] (required if
+ *               amax_in is NULL)
+ *   codes       [batch][rows][cols/2];  tile_scales [batch][rows/16][cols/16]
+ *   s_dec_out   device float[batch]
+ *   rows % 16 == 0, cols % 16 == 0, batch >= 1.
+ */
+FP4Q_API int fp4q_quantize_2d(const void* w_bf16, int64_t rows, int64_t cols, int64_t ld,
+                     int64_t batch, int64_t batch_stride,
+                     const float* amax_in, float* amax_ws,
+                     uint8_t* codes, uint8_t* tile_scales, float* s_dec_out,
+                     fp4q_stream_t stream);
+
+/*
+ * fp4q_requant_t_mxfp8_sr — dequantize, optionally transpose, optionally apply the 16-point
+ * random Hadamard transform, and quantize to MXFP8 with stochastic rounding.
+ * [VZ] §9-10 ("each saved tensor is dequantized, transposed and re-quantized to MXFP8 with
+ * SR"); [TML] "基于随机舍入的重量化"; [NV] "Random Hadamard Transforms" (wgrad operands);
+ * [AC] "The scaling math, worked" (power-of-two ceiling scale).
+ *   in_kind   FP4Q_IN_BF16: in = bf16 [rows][cols]; in_scales, in_s_dec unused (may be NULL)
+ *             FP4Q_IN_NVFP4_1D: in = codes [rows][cols/2], in_scales [rows][cols/16],
+ *                               in_s_dec = device float
+ *             FP4Q_IN_NVFP4_2D: in = codes [rows][cols/2], in_scales [rows/16][cols/16]
+ *   dequantized value (fp32) = (E2M1(code) * E4M3(scale)) * s_dec
+ *   transpose 0: output [rows][cols]; 1: output [cols][rows]. MXFP8 blocks of 32 and the
+ *             Hadamard groups of 16 run along the OUTPUT's contiguous dimension.
+ *   rht       0 / 1. The transform on each group of 16: y = (1/4) H16 (s o x), Sylvester H16,
+ *             bit i of rht_signs set -> s_i = -1; evaluated as butterflies at distances
+ *             1, 2, 4, 8 in fp32, then the exact multiply by 1/4.
+ *   per block of 32: e = the smallest integer with amax <= 448 * 2^e, clamped to [-127, 127];
+ *             out_e8m0 = e + 127; element = E4M3(x * 2^-e) rounded by `rounding`.
+ *   rounding  FP4Q_SR: floor(t/step + U) on the local E4M3 grid, U = R/2^16, where R is the
+ *             16-bit slice for the element's linear output index i of Philox4x32-10 with
+ *             key (seed lo32, seed hi32) and counter (i>>3 lo32, i>>3 hi32, tensor_tag, 0):
+ *             word (i>>1)&3, low half for even i, high half for odd i.
+ *             FP4Q_RNE: round to nearest, ties to even.
+ *   out_e4m3  [out_rows][out_cols] bytes; out_e8m0 [out_rows][out_cols/32] bytes
+ *   rows % 32 == 0 and cols % 32 == 0; for FP4Q_IN_NVFP4_2D also rows % 16 == 0.
+ *   in is 16-byte aligned; out_e4m3 is 16-byte aligned.
+ */
+FP4Q_API int fp4q_requant_t_mxfp8_sr(int in_kind, const void* in, const uint8_t* in_scales,
+                            const float* in_s_dec, int64_t rows, int64_t cols,
+                            int transpose, int rht, uint32_t rht_signs,
+                            int rounding, uint64_t seed, uint32_t tensor_tag,
+                            uint8_t* out_e4m3, uint8_t* out_e8m0, fp4q_stream_t stream);
+
+/*
+ * fp4q_rht16 — the 16-point random Hadamard transform on its own, along rows.
+ * [NV] "Random Hadamard Transforms"; [AC] "Hadamard rotations". Same arithmetic and order
+ * as the transform inside fp4q_requant_t_mxfp8_sr.
+ *   in        [rows][cols], in_dtype FP4Q_F32 or FP4Q_BF16, 16-byte aligned
+ *   out       [rows][cols] fp32, 16-byte aligned (may alias `in` when in_dtype == FP4Q_F32)
+ *   cols % 16 == 0.
+ */
+FP4Q_API int fp4q_rht16(const void* in, int in_dtype, float* out, int64_t rows, int64_t cols,
+               uint32_t signs, fp4q_stream_t stream);
+
+/*
+ * fp4q_gemm_nvfp4 — block-scaled NVFP4 x NVFP4 GEMM, D = A . B^T, FP32 accumulation on the
+ * tcgen05 tensor cores. [NV] "NVFP4 Format and Quantization Procedure", step 5:
+ *   D[m,n] = s_dec_a * s_dec_b * sum_blocks sa[m,blk] * sb[n,blk] * sum_{k in blk} a_k b_k
+ *   a, a_scales, a_s_dec    codes [M][K/2], E4M3 [M][K/16] (1D), device float
+ *   b, b_scales, b_s_dec    codes [groups][N][K/2]; scales [groups][N][K/16] (b_scale_kind
+ *                           FP4Q_SCALE_1D) or [groups][N/16][K/16] (FP4Q_SCALE_2D, each tile
+ *                           scale serves its 16 rows); b_s_dec device float[groups]
+ *   d, d_dtype              [M][N] FP4Q_F32 or FP4Q_BF16 (round to nearest even)
+ *   groups, group_row_offsets_host
+ *                           groups == 1: offsets may be NULL. groups > 1 (grouped GEMM, MoE
+ *                           experts): HOST int64 array of groups+1 ascending row offsets into
+ *                           A and D with offsets[0] = 0 and offsets[groups] = M; rows of group
+ *                           g multiply B[g]. groups <= 64.
+ *   M >= 1, N % 16 == 0, K % 256 == 0 (whole 256-value pipeline stages); a, b, a_scales,
+ *   b_scales and d 16-byte aligned.
+ */
+FP4Q_API int fp4q_gemm_nvfp4(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec,
+                    const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
+                    const float* b_s_dec, void* d, int d_dtype,
+                    int64_t M, int64_t N, int64_t K,
+                    int groups, const int64_t* group_row_offsets_host, fp4q_stream_t stream);
+
+/*
+ * fp4q_gemm_mxfp8 — block-scaled MXFP8 x MXFP8 GEMM, D = A . B^T, FP32 accumulation on the
+ * tcgen05 tensor cores (the dgrad and wgrad GEMMs of the backward pass). [VZ] §8 and §10:
+ * dx = g . w_q sums over N, dw = g^T . x_q sums over tokens; both operands carry their
+ * E8M0 block scales along the contraction dimension.
+ *   D[m,n] = sum_blk 2^(ea[m,blk]-127) * 2^(eb[n,blk]-127) * sum_{k in blk} a_k b_k
+ *   a, a_scales   E4M3 [M][K], E8M0 [M][K/32];  b, b_scales  E4M3 [N][K], E8M0 [N][K/32]
+ *   d, d_dtype    [M][N] FP4Q_F32 or FP4Q_BF16
+ *   M >= 1, N % 16 == 0, K % 128 == 0 (whole 128-value pipeline stages); a, b, d 16-byte
+ *   aligned; a_scales and b_scales 4-byte aligned.
+ */
+FP4Q_API int fp4q_gemm_mxfp8(const uint8_t* a, const uint8_t* a_scales,
+                    const uint8_t* b, const uint8_t* b_scales,
+                    void* d, int d_dtype, int64_t M, int64_t N, int64_t K,
+                    fp4q_stream_t stream);
+
+/*
+ * fp4q_device_status — synchronizes `stream`, then reads and clears the library's device-side
+ * error word. Returns FP4Q_ERR_TIMEOUT if a kernel's bounded wait (a GEMM pipeline barrier)
+ * gave up since the last call, FP4Q_ERR_CUDA if the stream reports an error, else FP4Q_OK.
+ * This is the only call that blocks the host.
+ */
+FP4Q_API int fp4q_device_status(fp4q_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4Q_H */

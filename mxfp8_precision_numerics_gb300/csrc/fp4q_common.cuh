@@ -1,0 +1,173 @@
+// fp4q_common.cuh — device-side building blocks of the NVFP4 / MXFP8 kernels (sm_103a).
+//
+// Number formats (4bit.vizuara.ai §3-6; "Pretraining Large Language Models with NVFP4",
+// "NVFP4 Format and Quantization Procedure"):
+//   E2M1  s|ee|m, bias 1, exponent 0 subnormal: magnitudes {0,.5,1,1.5,2,3,4,6}
+//   E4M3  s|eeee|mmm, bias 7, max 448 (0x7E), min subnormal 2^-9; 0x7F is NaN (never made)
+//   E8M0  2^(byte - 127)
+// Every fp32 operation of the quantization arithmetic goes through an explicit
+// round-to-nearest intrinsic so that no multiply-add is contracted and each result is
+// the single correctly rounded IEEE value the method's formulas name.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp4q {
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t h16) { return __uint_as_float(h16 << 16); }
+
+// ---------------------------------------------------------------------------------------
+// E4M3, round to nearest even with saturation to 448. Input any finite fp32.
+//   normal range (|v| >= 2^-6): keep 3 of the 23 mantissa bits with a nearest-even carry
+//   on the fp32 bit pattern (the carry may ripple into the exponent, which is exact);
+//   subnormal range: the value in units of 2^-9 is rounded to the nearest even integer.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3_rne_sat(float v) {
+    uint32_t u = __float_as_uint(v);
+    uint32_t s = (u >> 24) & 0x80u;
+    uint32_t a = u & 0x7FFFFFFFu;
+    uint32_t c;
+    if (a >= 0x43E00000u) {                       // |v| >= 448
+        c = 0x7Eu;
+    } else if (a >= 0x3C800000u) {                // |v| >= 2^-6: normal E4M3
+        uint32_t r = a + 0x7FFFFu + ((a >> 20) & 1u);
+        c = (r >> 20) - (120u << 3);              // rebias exponent 127 -> 7
+    } else {
+        float q = __fmul_rn(__uint_as_float(a), 512.0f);   // exact: power-of-two scale
+        c = (uint32_t)__float2int_rn(q);          // nearest even in [0, 8]
+    }
+    return s | c;
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+    uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    float mag = (e == 0) ? __fmul_rn((float)m, 0.001953125f)          // m * 2^-9
+                         : __uint_as_float(((e + 120u) << 23) | (m << 20));
+    return (c & 0x80u) ? -mag : mag;
+}
+
+// E2M1 magnitude of a 4-bit code (sign in bit 3).
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+    // bit pattern table of the eight magnitudes, four bits of fp32 exponent/mantissa each
+    // is not needed: decode arithmetically.
+    uint32_t e = (c >> 1) & 3u, m = c & 1u;
+    float mag = (e == 0) ? (m ? 0.5f : 0.0f) : __uint_as_float(((e + 126u) << 23) | (m << 22));
+    return (c & 8u) ? -mag : mag;
+}
+
+// ---------------------------------------------------------------------------------------
+// E2M1, round to nearest with ties to the even code, saturating at 6; the sign is kept
+// even when the magnitude rounds to zero. Decision thresholds are the midpoints between
+// neighbouring grid values; at an exact midpoint the even code wins.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e2m1_rne_alu(float v) {
+    float a = fabsf(v);
+    uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f)
+               + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
+    return c | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+// Hardware conversion of two fp32 values to two E2M1 codes (round to nearest, satfinite).
+// Used only where a device test has shown it equal to e2m1_rne_alu on every tie.
+__device__ __forceinline__ uint32_t e2m1x2_cvt_rn(float lo, float hi) {
+    uint32_t d;
+    asm("{.reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %2, %1; cvt.u32.u8 %0, t;}"
+        : "=r"(d) : "f"(lo), "f"(hi));
+    return d;   // low nibble = lo, high nibble = hi
+}
+
+// ---------------------------------------------------------------------------------------
+// MXFP8 block exponent, ceiling rule: the smallest integer e with amax <= 448 * 2^e,
+// clamped to [-127, 127] ("FP4 Training on Blackwell", "The scaling math, worked").
+// 448 = 1.75 * 2^8, so for amax = m * 2^E (m in [1,2)): e = E - 8 + (m > 1.75).
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ int mx_exponent(float amax) {
+    uint32_t u = __float_as_uint(amax) & 0x7FFFFFFFu;
+    if (u < 0x00800000u) return -127;             // zero or subnormal: far below 448*2^-127
+    int E = (int)(u >> 23) - 127;
+    int e = E - 8 + ((u & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^k as fp32 for k in [-127, 127] (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float exp2i(int k) {
+    return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// ---------------------------------------------------------------------------------------
+// E4M3 stochastic rounding of t (|t| <= 448): floor(t/step + U) on the local grid with
+// U = r16 / 2^16. Normal range: the 20 discarded mantissa bits F plus r16 << 4 carry into
+// the kept bits exactly when F/2^20 + U >= 1. Subnormal range: in units of 2^-9 the value
+// is m + f (m integer, f exact), rounded up when f >= 1 - U.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3_sr(float t, uint32_t r16) {
+    uint32_t u = __float_as_uint(t);
+    uint32_t s = (u >> 24) & 0x80u;
+    uint32_t a = u & 0x7FFFFFFFu;
+    uint32_t c;
+    if (a >= 0x43E00000u) {
+        c = 0x7Eu;
+    } else if (a >= 0x3C800000u) {
+        c = ((a + (r16 << 4)) >> 20) - (120u << 3);
+    } else {
+        float q = __fmul_rn(__uint_as_float(a), 512.0f);
+        float m = truncf(q);
+        float f = __fsub_rn(q, m);
+        float thr = __fmul_rn((float)(65536u - r16), 1.52587890625e-05f);   // (2^16 - r) / 2^16
+        c = (uint32_t)m + (f >= thr ? 1u : 0u);
+    }
+    return s | c;
+}
+
+// ---------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
+// SC'11): ten rounds of two 32x32->64 multiplies with the Weyl key schedule.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// The eight 16-bit random slices for output elements [8*blk, 8*blk + 8) of tensor `tag`.
+__device__ __forceinline__ uint4 sr_block8(uint64_t seed, uint32_t tag, uint64_t blk) {
+    return philox4x32_10(make_uint4((uint32_t)blk, (uint32_t)(blk >> 32), tag, 0u),
+                         (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+__device__ __forceinline__ uint32_t slice16(uint4 w, int j) {
+    uint32_t x = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;
+    return (j & 1) ? (x >> 16) : (x & 0xFFFFu);
+}
+
+// ---------------------------------------------------------------------------------------
+// 16-point random Hadamard transform of v[0..15] in place: signs, butterflies at
+// distances 1, 2, 4, 8 (Sylvester H16 = H2 (x) H8), then the exact scaling by 1/4.
+// ("Pretraining Large Language Models with NVFP4", "Random Hadamard Transforms".)
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void rht16_inplace(float* v, uint32_t signs) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if ((signs >> i) & 1u) v[i] = -v[i];
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if ((i & h) == 0) {
+                float a = v[i], b = v[i + h];
+                v[i] = __fadd_rn(a, b);
+                v[i + h] = __fsub_rn(a, b);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+}
+
+}  // namespace fp4q

@@ -1,0 +1,57 @@
+// fp4q_internal.h — launchers shared between the kernel translation units and the C ABI.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp4q {
+
+int num_sms();            // SM count of the current device (cached per device)
+bool use_hw_e2m1();       // convert E2M1 with the hardware cvt (shown equal to the ALU rule)
+
+cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int64_t batch,
+                        int64_t batch_stride, float* out, cudaStream_t st);
+cudaError_t launch_quantize_1d(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                               const float* amax, uint8_t* codes, uint8_t* scales, float* s_dec,
+                               cudaStream_t st);
+cudaError_t launch_quantize_2d(const uint16_t* w, int64_t rows, int64_t cols, int64_t ld,
+                               int64_t batch, int64_t batch_stride, const float* amax,
+                               uint8_t* codes, uint8_t* tile_scales, float* s_dec,
+                               cudaStream_t st);
+
+struct RequantArgs {
+    int in_kind;                 // 0 bf16, 1 NVFP4 1D, 2 NVFP4 2D
+    const void* in;
+    const uint8_t* in_scales;
+    const float* in_s_dec;
+    int64_t rows, cols;
+    int transpose, rht;
+    uint32_t rht_signs;
+    int rounding;                // 0 RNE, 1 SR
+    uint64_t seed;
+    uint32_t tag;
+    uint8_t* out_e4m3;
+    uint8_t* out_e8m0;
+};
+cudaError_t launch_requant(const RequantArgs& a, cudaStream_t st);
+cudaError_t launch_rht16(const void* in, int in_is_bf16, float* out, int64_t rows, int64_t cols,
+                         uint32_t signs, cudaStream_t st);
+
+struct GemmArgs {
+    int kind;                    // 0 NVFP4, 1 MXFP8
+    const uint8_t* a;
+    const uint8_t* a_scales;
+    const float* a_s_dec;        // NVFP4 only
+    const uint8_t* b;
+    const uint8_t* b_scales;
+    int b_scale_kind;            // NVFP4: 1 = 1D, 2 = 16x16 tiles
+    const float* b_s_dec;        // NVFP4 only, [groups]
+    void* d;
+    int d_bf16;
+    int64_t M, N, K;
+    int groups;
+    const int64_t* group_offsets;   // host, groups + 1 (NULL when groups == 1)
+};
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st);
+int read_and_clear_device_error(cudaStream_t st, int* flag);
+
+}  // namespace fp4q

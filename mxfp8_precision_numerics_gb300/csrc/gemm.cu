@@ -1,0 +1,520 @@
+// gemm.cu — block-scaled NVFP4 x NVFP4 and MXFP8 x MXFP8 GEMMs on the sm_103a tcgen05
+// tensor cores: D = A . B^T with FP32 accumulation in tensor memory.
+//
+// "Pretraining Large Language Models with NVFP4", "NVFP4 Format and Quantization
+// Procedure", step 5: the tensor core multiplies 16-value blocks of codes, scales each
+// partial sum by both blocks' E4M3 scales and accumulates in FP32; the per-tensor decode
+// scales are applied to the output afterwards. 4bit.vizuara.ai §7-8: a block-scaled GEMM
+// needs its blocks along the contraction dimension (K-major operands on both sides).
+// MXFP8 (dgrad / wgrad, 4bit.vizuara.ai §10): E4M3 operands with one E8M0 scale per 32.
+//
+// One CTA computes a 128 x 256 output tile (cta_group::1, M = 128, N = 256). Warp roles:
+//   warps 0-3  epilogue: tcgen05.ld of TMEM lanes 32w..32w+31 (rows), x alpha, store
+//   warp 4     TMA producer: A tile 128 rows x 128 B, B tile 256 rows x 128 B, 128B swizzle
+//   warp 5     TMEM allocator and MMA issuer (one elected lane): tcgen05.cp of the stage's
+//              scale atoms to TMEM, then 4 block-scaled tcgen05.mma, commit -> free stage
+//   warps 6,7  scale loaders for A and B: read the row-major scales of the next stage into
+//              registers and rewrite them into the 512-byte atoms the 32x128b.warpx4
+//              tensor-memory copy consumes (row m -> byte (m%32)*16 + (m/32)*4, 4 bytes of
+//              scales per row and MMA)
+// A 4-stage shared-memory ring connects them through mbarriers (full: TMA bytes + two
+// loader arrivals; empty: tcgen05.commit). Every wait is bounded: on timeout the kernel
+// raises the library's device error word and unwinds instead of hanging.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstring>
+#include "fp4q_common.cuh"
+#include "fp4q_internal.h"
+
+namespace fp4q {
+
+__device__ unsigned int g_device_error;      // bit 0: a bounded wait timed out
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kBM = 128, kBN = 256, kBKBytes = 128;
+constexpr int kThreads = 256;
+constexpr uint64_t kTimeoutNs = 1500000000ull;     // 1.5 s
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol = 0;                   // accumulator columns [0, 256)
+constexpr uint32_t kSfCol = 256;                  // scale-factor columns follow
+
+template <int kKind> struct Cfg;
+template <> struct Cfg<0> {   // NVFP4: K = 256 values (128 B) per stage, 4 MMAs of K = 64
+    static constexpr uint32_t kSfaBytes = 4 * 512, kSfbBytes = 8 * 512;
+    static constexpr uint32_t kSfColsPerStage = 48;   // SFA 4 x 4 + SFB 4 x 8
+    static constexpr int kValuesPerStage = 256;
+};
+template <> struct Cfg<1> {   // MXFP8: K = 128 values per stage, 4 MMAs of K = 32
+    static constexpr uint32_t kSfaBytes = 512, kSfbBytes = 2 * 512;
+    static constexpr uint32_t kSfColsPerStage = 12;   // SFA 4 + SFB 8 (4 bytes = 4 MMAs)
+    static constexpr int kValuesPerStage = 128;
+};
+
+constexpr uint32_t kABytes = kBM * kBKBytes;      // 16 KB
+constexpr uint32_t kBBytes = kBN * kBKBytes;      // 32 KB
+
+template <int kKind>
+__host__ __device__ constexpr uint32_t stage_bytes() {
+    return ((kABytes + kBBytes + Cfg<kKind>::kSfaBytes + Cfg<kKind>::kSfbBytes + 1023) / 1024) * 1024;
+}
+template <int kKind>
+__host__ __device__ constexpr uint32_t smem_bytes() { return kStages * stage_bytes<kKind>() + 1024 + 256; }
+
+struct Params {
+    CUtensorMap tma_a;
+    CUtensorMap tma_b;
+    const uint8_t* a_sc;
+    const uint8_t* b_sc;
+    int64_t sc_ld;             // scale bytes per row (K/16 NVFP4, K/32 MXFP8)
+    int b_sc_2d;
+    const float* a_s_dec;
+    const float* b_s_dec;
+    void* d;
+    int d_bf16;
+    int64_t M, N, K;
+    int num_kb;
+    int n_tiles;
+    int groups;
+    int64_t goff[65];
+    int gtile[65];
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Bounded wait on the phase with the given parity. false = gave up (error word raised).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0 && globaltimer() - t0 > kTimeoutNs) {
+            atomicOr(&g_device_error, 1u);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%3, %4}], [%2];"
+                 ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void mma_nvfp4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t acc) {
+    asm volatile("{.reg .pred p; setp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+                 " [%0], %1, %2, %3, [%5], [%6], p;}"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb) : "memory");
+}
+__device__ __forceinline__ void mma_mxfp8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t acc) {
+    asm volatile("{.reg .pred p; setp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+                 " [%0], %1, %2, %3, [%5], [%6], p;}"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb) : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32"
+                 " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+                   "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+                   "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, K-major operand with 128-byte swizzle: 8-row core
+// groups 1024 bytes apart (stride byte offset), leading byte offset unused, version 1.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+// Descriptor of one 32 x 16-byte scale atom (no swizzle; 8-row groups 128 bytes apart).
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (8ull << 32) | (1ull << 46);
+}
+
+// Instruction descriptors (M = 128, N = 256, K-major A and B, dense).
+//   bits 7-9 / 10-12 operand formats, 17-22 N >> 3, 23 scale type (0 UE4M3, 1 UE8M0),
+//   24-28 M >> 4, 4-5 B scale-factor id, 29-30 A scale-factor id.
+constexpr uint32_t kIdescNvfp4 = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                                 (0u << 23) | ((uint32_t)(kBM >> 4) << 24);
+constexpr uint32_t kIdescMxfp8 = (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                                 (1u << 23) | ((uint32_t)(kBM >> 4) << 24);
+
+__device__ __forceinline__ uint4 ld_sc16(const uint8_t* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int kKind>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr uint32_t kStage = stage_bytes<kKind>();
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStage);
+    uint64_t* empty = full + kStages;
+    uint64_t* accum = empty + kStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+    int* issued = reinterpret_cast<int*>(tmem_slot + 1);     // stages the producer loaded
+    int* consumed = issued + 1;                              // stages the MMA issuer used
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- tile decode: linear tile -> (group, m0, n0)
+    const int t = blockIdx.x;
+    const int mt = t / p.n_tiles, nt = t - mt * p.n_tiles;
+    int g = 0;
+    while (g + 1 < p.groups && p.gtile[g + 1] <= mt) ++g;
+    const int64_t m0 = p.goff[g] + (int64_t)(mt - p.gtile[g]) * kBM;
+    const int64_t m_end = p.goff[g + 1];
+    const int64_t n0 = (int64_t)nt * kBN;
+    const int64_t brow0 = (int64_t)g * p.N + n0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 3);      // TMA arrive.expect_tx + A-scale + B-scale loaders
+            mbar_init(&empty[s], 1);     // tcgen05.commit
+        }
+        mbar_init(accum, 1);
+        *issued = 0;
+        *consumed = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tma_a) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tma_b) : "memory");
+            int kb = 0;
+            for (; kb < p.num_kb; ++kb) {
+                const int s = kb % kStages;
+                const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
+                if (!mbar_wait(&empty[s], ph ^ 1u)) break;
+                uint8_t* st = smem + s * kStage;
+                mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
+                tma_load_2d(&p.tma_a, &full[s], st, kb * kBKBytes, (int32_t)m0);
+                tma_load_2d(&p.tma_b, &full[s], st + kABytes, kb * kBKBytes, (int32_t)brow0);
+            }
+            *issued = kb;
+        }
+    } else if (warp == 6 || warp == 7) {
+        // ------------------------------------------------ scale loaders (A: warp 6, B: warp 7)
+        const bool is_b = (warp == 7);
+        constexpr int kMaxR = 8;                       // rows per lane: A 4, B 8
+        const int R = is_b ? 8 : 4;
+        const uint8_t* base;
+        int64_t row_lim;
+        if (!is_b) {
+            base = p.a_sc;
+            row_lim = p.M;
+        } else {
+            base = p.b_sc + (p.b_sc_2d ? (int64_t)g * (p.N / 16) * p.sc_ld : (int64_t)g * p.N * p.sc_ld);
+            row_lim = p.N;
+        }
+        const int64_t r0 = is_b ? n0 : m0;
+        const uint32_t sf_off = kABytes + kBBytes + (is_b ? Cfg<kKind>::kSfaBytes : 0);
+        uint4 cur[kMaxR], nxt[kMaxR];
+        auto load = [&](int kb, uint4 (&dst)[kMaxR]) {
+#pragma unroll
+            for (int q = 0; q < kMaxR; ++q) {
+                dst[q] = make_uint4(0, 0, 0, 0);
+                if (q < R) {
+                    const int64_t row = r0 + lane + 32 * q;
+                    if (row < row_lim) {
+                        const int64_t srow = (is_b && p.b_sc_2d) ? (row >> 4) : row;
+                        const uint8_t* src = base + srow * p.sc_ld;
+                        if (kKind == 0) {
+                            dst[q] = ld_sc16(src + (int64_t)kb * 16);
+                        } else {
+                            dst[q].x = __ldg(reinterpret_cast<const uint32_t*>(src + (int64_t)kb * 4));
+                        }
+                    }
+                }
+            }
+        };
+        load(0, cur);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            const int s = kb % kStages;
+            const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
+            if (kb + 1 < p.num_kb) load(kb + 1, nxt);
+            if (!mbar_wait(&empty[s], ph ^ 1u)) break;
+            uint8_t* sf = smem + s * kStage + sf_off;
+            if (kKind == 0) {
+                // atom (j, h): rows 128h + [0,128) of MMA j; lane l writes rows l, l+32, l+64, l+96
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && !is_b) break;
+                    const uint4 q0 = cur[4 * h], q1 = cur[4 * h + 1], q2 = cur[4 * h + 2], q3 = cur[4 * h + 3];
+                    const int nh = is_b ? 2 : 1;
+                    *reinterpret_cast<uint4*>(sf + (0 * nh + h) * 512 + lane * 16) = make_uint4(q0.x, q1.x, q2.x, q3.x);
+                    *reinterpret_cast<uint4*>(sf + (1 * nh + h) * 512 + lane * 16) = make_uint4(q0.y, q1.y, q2.y, q3.y);
+                    *reinterpret_cast<uint4*>(sf + (2 * nh + h) * 512 + lane * 16) = make_uint4(q0.z, q1.z, q2.z, q3.z);
+                    *reinterpret_cast<uint4*>(sf + (3 * nh + h) * 512 + lane * 16) = make_uint4(q0.w, q1.w, q2.w, q3.w);
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (h == 1 && !is_b) break;
+                    *reinterpret_cast<uint4*>(sf + h * 512 + lane * 16) =
+                        make_uint4(cur[4 * h].x, cur[4 * h + 1].x, cur[4 * h + 2].x, cur[4 * h + 3].x);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[s]);
+#pragma unroll
+            for (int q = 0; q < kMaxR; ++q) cur[q] = nxt[q];
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int kb = 0;
+            for (; kb < p.num_kb; ++kb) {
+                const int s = kb % kStages;
+                const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
+                if (!mbar_wait(&full[s], ph)) break;
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + s * kStage);
+                const uint32_t sb = sa + kABytes;
+                const uint32_t ssf = sb + kBBytes;
+                const uint32_t sf_col = tmem + kSfCol + (uint32_t)s * Cfg<kKind>::kSfColsPerStage;
+                if (kKind == 0) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) tc_cp_sf(sf_col + 4 * j, desc_sf(ssf + j * 512));
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            tc_cp_sf(sf_col + 16 + 8 * j + 4 * h,
+                                     desc_sf(ssf + Cfg<0>::kSfaBytes + (2 * j + h) * 512));
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma_nvfp4(tmem + kAccCol, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
+                                  kIdescNvfp4, sf_col + 4 * j, sf_col + 16 + 8 * j,
+                                  (kb | j) ? 1u : 0u);
+                } else {
+                    tc_cp_sf(sf_col, desc_sf(ssf));
+                    tc_cp_sf(sf_col + 4, desc_sf(ssf + Cfg<1>::kSfaBytes));
+                    tc_cp_sf(sf_col + 8, desc_sf(ssf + Cfg<1>::kSfaBytes + 512));
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma_mxfp8(tmem + kAccCol, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
+                                  kIdescMxfp8 | ((uint32_t)j << 29) | ((uint32_t)j << 4),
+                                  sf_col, sf_col + 4, (kb | j) ? 1u : 0u);
+                }
+                tc_commit(&empty[s]);
+            }
+            *consumed = kb;
+            // arrives once every MMA issued above has completed (also after a timeout, so
+            // that tensor memory is never released under a running MMA)
+            tc_commit(accum);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue warps 0-3
+        const bool ok = mbar_wait(accum, 0);
+        tc_fence_after();
+        if (ok) {
+            float alpha = 1.0f;
+            if (kKind == 0) alpha = __fmul_rn(p.a_s_dec[0], p.b_s_dec[g]);
+            const int64_t row = m0 + warp * 32 + lane;
+            const bool row_ok = row < m_end;
+#pragma unroll 1
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + kAccCol + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
+                const int64_t col = n0 + c * 32;
+                if (!row_ok || col >= p.N) continue;
+                const bool full32 = col + 32 <= p.N;
+                if (p.d_bf16) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha),
+                                                                  __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
+                        pk[i] = *reinterpret_cast<uint32_t*>(&h2);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + row * p.N + col);
+                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    if (full32) {
+                        dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+                        dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.N + col);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (i >= 4 && !full32) break;
+                        dst[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
+                                             __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
+                                             __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
+                                             __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4 && lane == 0) {
+        // after a timeout: wait (bounded) for TMA copies that were issued but never consumed,
+        // so that no copy lands in shared memory after the CTA has exited
+        for (int kb = *consumed; kb < *issued; ++kb)
+            if (!mbar_wait(&full[kb % kStages], (uint32_t)(kb / kStages) & 1u)) break;
+    }
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// 2D uint8 tensor map: [rows][row_bytes], box {128 B, box_rows}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)kBKBytes, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int kKind>
+cudaError_t launch_kind(const GemmArgs& a, cudaStream_t st) {
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem_bytes<kKind>());
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    Params p;
+    memset(&p, 0, sizeof(p));
+    const uint64_t kbytes = kKind == 0 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
+    if (!make_map(&p.tma_a, a.a, kbytes, (uint64_t)a.M, kBM)) return cudaErrorInvalidValue;
+    if (!make_map(&p.tma_b, a.b, kbytes, (uint64_t)a.N * (uint64_t)a.groups, kBN)) return cudaErrorInvalidValue;
+    p.a_sc = a.a_scales;
+    p.b_sc = a.b_scales;
+    p.sc_ld = kKind == 0 ? a.K / 16 : a.K / 32;
+    p.b_sc_2d = (kKind == 0 && a.b_scale_kind == 2) ? 1 : 0;
+    p.a_s_dec = a.a_s_dec;
+    p.b_s_dec = a.b_s_dec;
+    p.d = a.d;
+    p.d_bf16 = a.d_bf16;
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.num_kb = (int)(a.K / Cfg<kKind>::kValuesPerStage);
+    p.n_tiles = (int)((a.N + kBN - 1) / kBN);
+    p.groups = a.groups;
+    int64_t tiles_m = 0;
+    for (int gi = 0; gi < a.groups; ++gi) {
+        const int64_t lo = a.groups == 1 ? 0 : a.group_offsets[gi];
+        const int64_t hi = a.groups == 1 ? a.M : a.group_offsets[gi + 1];
+        p.goff[gi] = lo;
+        p.gtile[gi] = (int)tiles_m;
+        tiles_m += (hi - lo + kBM - 1) / kBM;
+    }
+    p.goff[a.groups] = a.M;
+    p.gtile[a.groups] = (int)tiles_m;
+    const int64_t tiles = tiles_m * p.n_tiles;
+    if (tiles <= 0) return cudaSuccess;
+    gemm_kernel<kKind><<<(unsigned)tiles, kThreads, smem_bytes<kKind>(), st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
+    return a.kind == 0 ? launch_kind<0>(a, st) : launch_kind<1>(a, st);
+}
+
+int read_and_clear_device_error(cudaStream_t st, int* flag) {
+    if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return -1;
+    if (v && cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return -1;
+    *flag = (int)v;
+    return 0;
+}
+
+}  // namespace fp4q

@@ -444,15 +444,16 @@ EXPORT void orc_mxfp8_block(const float* v, int rounding, uint64_t seed, uint32_
 /* Output: transpose ? [cols][rows] : [rows][cols], E8M0 per 32 along the       */
 /*         output's contiguous dimension.                                      */
 /* ------------------------------------------------------------------------- */
-EXPORT void orc_requant_mxfp8(int in_kind, const void* in, const uint8_t* in_scales, float s_dec,
-                              int64_t rows, int64_t cols, int transpose, int rht, uint32_t rht_signs,
-                              int rounding, uint64_t seed, uint32_t tag,
-                              uint8_t* out_e4m3, uint8_t* out_e8m0)
+/* Output rows [orow_begin, orow_end) only; out_e4m3 / out_e8m0 hold just those rows. */
+EXPORT void orc_requant_mxfp8_rows(int in_kind, const void* in, const uint8_t* in_scales, float s_dec,
+                                   int64_t rows, int64_t cols, int transpose, int rht, uint32_t rht_signs,
+                                   int rounding, uint64_t seed, uint32_t tag,
+                                   int64_t orow_begin, int64_t orow_end,
+                                   uint8_t* out_e4m3, uint8_t* out_e8m0)
 {
-    int64_t orows = transpose ? cols : rows;
     int64_t ocols = transpose ? rows : cols;
     float v[32];
-    for (int64_t orow = 0; orow < orows; ++orow) {
+    for (int64_t orow = orow_begin; orow < orow_end; ++orow) {
         for (int64_t ob = 0; ob < ocols / 32; ++ob) {
             for (int i = 0; i < 32; ++i) {
                 int64_t oc = ob * 32 + i;
@@ -463,8 +464,18 @@ EXPORT void orc_requant_mxfp8(int in_kind, const void* in, const uint8_t* in_sca
                                                rows, cols, r, c);
             }
             if (rht) { orc_rht16_group(v, rht_signs); orc_rht16_group(v + 16, rht_signs); }
+            int64_t lr = orow - orow_begin;
             orc_mxfp8_block(v, rounding, seed, tag, (uint64_t)(orow * ocols + ob * 32),
-                            &out_e4m3[orow * ocols + ob * 32], &out_e8m0[orow * (ocols / 32) + ob]);
+                            &out_e4m3[lr * ocols + ob * 32], &out_e8m0[lr * (ocols / 32) + ob]);
         }
     }
+}
+
+EXPORT void orc_requant_mxfp8(int in_kind, const void* in, const uint8_t* in_scales, float s_dec,
+                              int64_t rows, int64_t cols, int transpose, int rht, uint32_t rht_signs,
+                              int rounding, uint64_t seed, uint32_t tag,
+                              uint8_t* out_e4m3, uint8_t* out_e8m0)
+{
+    orc_requant_mxfp8_rows(in_kind, in, in_scales, s_dec, rows, cols, transpose, rht, rht_signs,
+                           rounding, seed, tag, 0, transpose ? cols : rows, out_e4m3, out_e8m0);
 }

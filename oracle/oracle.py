@@ -78,6 +78,11 @@ def lib():
         L.orc_mxfp8_block.restype = None
         L.orc_mxfp8_block.argtypes = [_f32p, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32,
                                       ctypes.c_uint64, _u8p, _u8p]
+        L.orc_requant_mxfp8_rows.restype = None
+        L.orc_requant_mxfp8_rows.argtypes = [ctypes.c_int, ctypes.c_void_p, _u8p, ctypes.c_float,
+                                             _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
+                                             ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32, _i64, _i64,
+                                             _u8p, _u8p]
         L.orc_requant_mxfp8.restype = None
         L.orc_requant_mxfp8.argtypes = [ctypes.c_int, ctypes.c_void_p, _u8p, ctypes.c_float,
                                         _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
@@ -228,8 +233,9 @@ def mxfp8_block(v, rounding=RNE, seed=0, tag=0, out_idx0=0):
 
 
 def requant_mxfp8(in_kind, data, scales, s_dec, rows, cols, transpose, rht, rht_signs,
-                  rounding, seed, tag):
-    """Dequantize -> [transpose] -> [RHT16] -> MXFP8 -> (e4m3, e8m0)."""
+                  rounding, seed, tag, out_rows=None):
+    """Dequantize -> [transpose] -> [RHT16] -> MXFP8 -> (e4m3, e8m0).
+    out_rows=(begin, end) computes only those output rows."""
     if in_kind == IN_BF16:
         data = _c(data, np.uint16)
         sc = None
@@ -238,11 +244,12 @@ def requant_mxfp8(in_kind, data, scales, s_dec, rows, cols, transpose, rht, rht_
         scales = _c(scales, np.uint8)
         sc = _p(scales, _u8p)
     orows, ocols = (cols, rows) if transpose else (rows, cols)
-    e4 = np.zeros((orows, ocols), np.uint8)
-    e8 = np.zeros((orows, ocols // 32), np.uint8)
-    lib().orc_requant_mxfp8(in_kind, data.ctypes.data, sc, float(s_dec), rows, cols,
-                            int(bool(transpose)), int(bool(rht)), int(rht_signs), rounding,
-                            int(seed), int(tag), _p(e4, _u8p), _p(e8, _u8p))
+    b, e = (0, orows) if out_rows is None else out_rows
+    e4 = np.zeros((e - b, ocols), np.uint8)
+    e8 = np.zeros((e - b, ocols // 32), np.uint8)
+    lib().orc_requant_mxfp8_rows(in_kind, data.ctypes.data, sc, float(s_dec), rows, cols,
+                                 int(bool(transpose)), int(bool(rht)), int(rht_signs), rounding,
+                                 int(seed), int(tag), b, e, _p(e4, _u8p), _p(e8, _u8p))
     return e4, e8
 
 

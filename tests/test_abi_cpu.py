@@ -1,0 +1,108 @@
+"""CPU checks of the C-ABI library: it loads, it exports every symbol include/fp4q.h
+declares, and its host-side validation rejects bad arguments before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "fp4q.h")
+
+
+@pytest.fixture(scope="module")
+def F():
+    import __graft_entry__ as g
+    g.build()
+    from mxfp8_precision_numerics_gb300 import fp4q
+    return fp4q
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"FP4Q_API\s+[\w\s\*]+?\b(fp4q_\w+)\s*\(", text)
+
+
+def test_header_declares_the_six_entry_points():
+    syms = set(declared_symbols())
+    for name in ("fp4q_quantize_1d", "fp4q_quantize_2d", "fp4q_requant_t_mxfp8_sr", "fp4q_rht16",
+                 "fp4q_gemm_nvfp4", "fp4q_gemm_mxfp8"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(F):
+    lib = ctypes.CDLL(F.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(F):
+    assert F.version() == 100
+    for s in range(8):
+        assert F.status_str(s).startswith("FP4Q")
+    assert "unknown" in F.status_str(99)
+
+
+def _lib(F):
+    return F._lib
+
+
+def test_validation_rejects_bad_arguments_without_touching_cuda(F):
+    L = _lib(F)
+    p = ctypes.c_void_p(16)            # an aligned dummy address: never dereferenced
+    q = ctypes.c_void_p(17)            # misaligned
+    n = None
+    # quantize_1d: NULL, shape, alignment
+    assert L.fp4q_quantize_1d(n, 16, 32, 32, n, p, p, p, p, n) == F.ERR_NULL
+    assert L.fp4q_quantize_1d(p, 16, 32, 32, n, n, p, p, p, n) == F.ERR_NULL   # no amax source
+    assert L.fp4q_quantize_1d(p, 16, 40, 40, n, p, p, p, p, n) == F.ERR_SHAPE
+    assert L.fp4q_quantize_1d(p, 0, 32, 32, n, p, p, p, p, n) == F.ERR_SHAPE
+    assert L.fp4q_quantize_1d(p, 16, 32, 16, n, p, p, p, p, n) == F.ERR_SHAPE  # ld < cols
+    assert L.fp4q_quantize_1d(q, 16, 32, 32, n, p, p, p, p, n) == F.ERR_ALIGN
+    assert L.fp4q_quantize_1d(p, 16, 32, 36, n, p, p, p, p, n) == F.ERR_ALIGN  # ld % 8
+    # quantize_2d
+    assert L.fp4q_quantize_2d(p, 24, 32, 32, 1, 0, n, p, p, p, p, n) == F.ERR_SHAPE
+    assert L.fp4q_quantize_2d(p, 32, 32, 32, 2, 16, n, p, p, p, p, n) == F.ERR_SHAPE  # overlapping batch
+    assert L.fp4q_quantize_2d(p, 32, 32, 32, 1, 0, n, p, n, p, p, n) == F.ERR_NULL
+    # requant
+    assert L.fp4q_requant_t_mxfp8_sr(3, p, p, p, 32, 32, 1, 0, 0, 1, 0, 0, p, p, n) == F.ERR_ARG
+    assert L.fp4q_requant_t_mxfp8_sr(0, p, n, n, 32, 32, 2, 0, 0, 1, 0, 0, p, p, n) == F.ERR_ARG
+    assert L.fp4q_requant_t_mxfp8_sr(0, p, n, n, 32, 32, 1, 0, 0, 2, 0, 0, p, p, n) == F.ERR_ARG
+    assert L.fp4q_requant_t_mxfp8_sr(0, p, n, n, 32, 32, 1, 1, 1 << 16, 1, 0, 0, p, p, n) == F.ERR_ARG
+    assert L.fp4q_requant_t_mxfp8_sr(1, p, n, p, 32, 32, 1, 0, 0, 1, 0, 0, p, p, n) == F.ERR_NULL
+    assert L.fp4q_requant_t_mxfp8_sr(0, p, n, n, 48, 32, 1, 0, 0, 1, 0, 0, p, p, n) == F.ERR_SHAPE
+    assert L.fp4q_requant_t_mxfp8_sr(0, p, n, n, 32, 32, 1, 0, 0, 1, 0, 0, q, p, n) == F.ERR_ALIGN
+    # rht16
+    assert L.fp4q_rht16(p, 2, p, 4, 16, 0, n) == F.ERR_ARG
+    assert L.fp4q_rht16(p, 0, p, 4, 24, 0, n) == F.ERR_SHAPE
+    assert L.fp4q_rht16(p, 0, q, 4, 16, 0, n) == F.ERR_ALIGN
+    # gemm_nvfp4
+    g = L.fp4q_gemm_nvfp4
+    assert g(p, p, p, p, p, 3, p, p, 0, 128, 256, 256, 1, None, n) == F.ERR_ARG
+    assert g(p, p, p, p, p, 1, p, p, 2, 128, 256, 256, 1, None, n) == F.ERR_ARG
+    assert g(p, p, p, p, p, 1, p, p, 0, 128, 256, 128, 1, None, n) == F.ERR_SHAPE   # K % 256
+    assert g(p, p, p, p, p, 1, p, p, 0, 128, 24, 256, 1, None, n) == F.ERR_SHAPE    # N % 16
+    assert g(p, p, p, p, p, 1, p, p, 0, 128, 256, 256, 0, None, n) == F.ERR_ARG     # groups
+    assert g(p, p, p, p, p, 1, p, p, 0, 128, 256, 256, 2, None, n) == F.ERR_NULL    # offsets
+    offs = (ctypes.c_int64 * 3)(0, 100, 120)
+    assert g(p, p, p, p, p, 1, p, p, 0, 128, 256, 256, 2, offs, n) == F.ERR_SHAPE   # last != M
+    offs = (ctypes.c_int64 * 3)(0, 100, 64)
+    assert g(p, p, p, p, p, 1, p, p, 0, 64, 256, 256, 2, offs, n) == F.ERR_SHAPE    # descending
+    assert g(q, p, p, p, p, 1, p, p, 0, 128, 256, 256, 1, None, n) == F.ERR_ALIGN
+    # gemm_mxfp8
+    m = L.fp4q_gemm_mxfp8
+    assert m(p, p, p, p, p, 0, 128, 256, 96, n) == F.ERR_SHAPE
+    assert m(p, p, p, p, n, 0, 128, 256, 128, n) == F.ERR_NULL
+    assert m(p, ctypes.c_void_p(18), p, p, p, 0, 128, 256, 128, n) == F.ERR_ALIGN
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    """The CUDA library and its binding never reach the oracle or a CPU path."""
+    pkg = os.path.join(ROOT, "mxfp8_precision_numerics_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "liboracle" not in text, f
