@@ -20,9 +20,10 @@ int num_sms() {
     return cached;
 }
 
-// The E2M1 conversion path. The hardware cvt is used only after a device test showed it to
-// agree with the round-to-nearest-even ALU rule on every tie of the grid.
-bool use_hw_e2m1() { return false; }
+// The E2M1 conversion path: the hardware cvt.rn.satfinite.e2m1x2 (one instruction per two
+// values). A device test checks it against the oracle's round-to-nearest-even rule on every
+// tie of the grid, on saturation and on a dense sweep; the ALU rule stays as the reference.
+bool use_hw_e2m1() { return true; }
 
 }  // namespace fp4q
 

@@ -65,6 +65,13 @@ def test_e2m1_encoder_matches_oracle(P, orc):
     torch.cuda.synchronize()
     want = np.array([orc.e2m1_encode_rne(v) for v in x], dtype=np.uint8)
     assert_bytes_equal(alu.cpu().numpy(), want, "E2M1 encoder (ALU)")
+    # the hardware conversion the quantizers use: same codes, including every tie (the pages
+    # report a hardware that breaks ties toward zero; on this device it must be to even),
+    # with the first source operand in the high nibble
+    lo, hi = lo.cpu().numpy(), hi.cpu().numpy()
+    assert_bytes_equal(lo & 15, want, "E2M1 hardware cvt (low nibble)")
+    assert_bytes_equal(lo >> 4, np.zeros_like(want), "E2M1 hardware cvt (other nibble)")
+    assert_bytes_equal(hi >> 4, want, "E2M1 hardware cvt (high nibble)")
 
 
 def test_e4m3_encoder_matches_oracle(P, orc):
@@ -79,6 +86,11 @@ def test_e4m3_encoder_matches_oracle(P, orc):
     lib = orc.lib()
     want = np.fromiter((lib.orc_e4m3_encode_rne_sat(float(v)) for v in x), dtype=np.uint8, count=n)
     assert_bytes_equal(alu.cpu().numpy(), want, "E4M3 encoder (ALU)")
+    # the hardware E4M3 conversion agrees too (first operand -> high byte)
+    h1 = h1.cpu().numpy().view(np.uint16)
+    h2 = h2.cpu().numpy().view(np.uint16)
+    assert_bytes_equal((h1 >> 8).astype(np.uint8), want, "E4M3 hardware cvt (high byte)")
+    assert_bytes_equal((h2 & 0xFF).astype(np.uint8), want, "E4M3 hardware cvt (low byte)")
 
 
 def test_e4m3_stochastic_rounding_matches_oracle(P, orc):
