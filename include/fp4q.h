@@ -111,6 +111,29 @@ FP4Q_API int fp4q_quantize_2d(const void* w_bf16, int64_t rows, int64_t cols, in
                      fp4q_stream_t stream);
 
 /*
+ * fp4q_quantize_2d_noalloc — fp4q_quantize_2d for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point: it is an interface convenience.
+ * Some callers cannot call cudaMalloc: a plugin whose host framework owns every device buffer
+ * and offers no workspace, or a latency-critical caller that must avoid cudaMalloc because it
+ * can synchronize the device. Here the per-tensor amax workspace is a fixed array inside the
+ * library (FP4Q_NOALLOC_MAX_BATCH floats, 4 KiB per device, kept until the process exits); the
+ * caller passes only inputs and outputs, with the same meaning, layout and results as
+ * fp4q_quantize_2d computing its own amax.
+ *   batch > FP4Q_NOALLOC_MAX_BATCH is rejected with FP4Q_ERR_SHAPE before any launch.
+ *   The first call on a device looks up the array's device address (once per device, with
+ *   that device current); make that first call before any stream capture.
+ *   Every call on a device shares the array: calls whose work may overlap on the GPU (two
+ *   streams without ordering between them) race on it. Calls ordered on one stream are safe;
+ *   each call clears the part it uses before accumulating the amax.
+ *   The library allocates nothing for this call.
+ */
+#define FP4Q_NOALLOC_MAX_BATCH 1024
+FP4Q_API int fp4q_quantize_2d_noalloc(const void* w_bf16, int64_t rows, int64_t cols, int64_t ld,
+                                      int64_t batch, int64_t batch_stride,
+                                      uint8_t* codes, uint8_t* tile_scales, float* s_dec_out,
+                                      fp4q_stream_t stream);
+
+/*
  * fp4q_requant_t_mxfp8_sr — dequantize, optionally transpose, optionally apply the 16-point
  * random Hadamard transform, and quantize to MXFP8 with stochastic rounding.
  * [VZ] §9-10 ("each saved tensor is dequantized, transposed and re-quantized to MXFP8 with

@@ -23,6 +23,7 @@ IN_BF16, IN_NVFP4_1D, IN_NVFP4_2D = 0, 1, 2
 RNE, SR = 0, 1
 F32, BF16 = 0, 1
 SCALE_1D, SCALE_2D = 1, 2
+NOALLOC_MAX_BATCH = 1024      # FP4Q_NOALLOC_MAX_BATCH
 
 # tensor tags of the four backward quantizations (stochastic-rounding counter streams)
 TAG_WT, TAG_DY_ROWS, TAG_DY_T, TAG_XT = 1, 2, 3, 4
@@ -45,6 +46,7 @@ _SIGS = {
     "fp4q_version": (_int, []),
     "fp4q_quantize_1d": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "fp4q_quantize_2d": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "fp4q_quantize_2d_noalloc": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
     "fp4q_requant_t_mxfp8_sr": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _int, _u32, _int, _u64,
                                        _u32, _vp, _vp, _vp]),
     "fp4q_rht16": (_int, [_vp, _int, _vp, _i64, _i64, _u32, _vp]),
@@ -98,6 +100,15 @@ def fp4q_quantize_2d(w, rows, cols, ld, batch, batch_stride, amax_in, amax_ws, c
     _check(_lib.fp4q_quantize_2d(_ptr(w), rows, cols, ld, batch, batch_stride, _ptr(amax_in),
                                  _ptr(amax_ws), _ptr(codes), _ptr(tile_scales), _ptr(s_dec_out),
                                  _stream(stream)), "fp4q_quantize_2d")
+
+
+def fp4q_quantize_2d_noalloc(w, rows, cols, ld, batch, batch_stride, codes, tile_scales, s_dec_out,
+                             stream=None):
+    """fp4q_quantize_2d with the amax workspace inside the library (for callers that cannot
+    allocate device memory); batch <= NOALLOC_MAX_BATCH."""
+    _check(_lib.fp4q_quantize_2d_noalloc(_ptr(w), rows, cols, ld, batch, batch_stride, _ptr(codes),
+                                         _ptr(tile_scales), _ptr(s_dec_out), _stream(stream)),
+           "fp4q_quantize_2d_noalloc")
 
 
 def fp4q_requant_t_mxfp8_sr(in_kind, inp, in_scales, in_s_dec, rows, cols, transpose, rht, rht_signs,
