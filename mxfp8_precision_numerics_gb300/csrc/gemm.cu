@@ -9,17 +9,23 @@
 // MXFP8 (dgrad / wgrad, 4bit.vizuara.ai §10): E4M3 operands with one E8M0 scale per 32.
 //
 // One CTA computes a 128 x 256 output tile (cta_group::1, M = 128, N = 256). Warp roles:
-//   warps 0-3  epilogue: tcgen05.ld of TMEM lanes 32w..32w+31 (rows), x alpha, store
-//   warp 4     TMA producer: A tile 128 rows x 128 B, B tile 256 rows x 128 B, 128B swizzle
-//   warp 5     TMEM allocator and MMA issuer (one elected lane): tcgen05.cp of the stage's
-//              scale atoms to TMEM, then 4 block-scaled tcgen05.mma, commit -> free stage
-//   warps 6,7  scale loaders for A and B: read the row-major scales of the next stage into
-//              registers and rewrite them into the 512-byte atoms the 32x128b.warpx4
-//              tensor-memory copy consumes (row m -> byte (m%32)*16 + (m/32)*4, 4 bytes of
-//              scales per row and MMA)
-// A 4-stage shared-memory ring connects them through mbarriers (full: TMA bytes + two
-// loader arrivals; empty: tcgen05.commit). Every wait is bounded: on timeout the kernel
-// raises the library's device error word and unwinds instead of hanging.
+//   warp 4     producer: lane 0 loads the A (128 rows x 128 B) and B (256 rows x 128 B) tiles
+//              of a stage with TMA (128-byte swizzle); all 32 lanes cp.async the stage's scale
+//              rows (16 B per row for NVFP4, 4 B for MXFP8) into the stage's staging area. Both
+//              complete the stage's `full` barrier (TMA transaction bytes + cp.async arrivals).
+//   warps 0-3  scale writers during the main loop, epilogue after it. The tensor core reads
+//              the scale of row r (A rows; B rows n0 + r) from TMEM lane r mod 32 and column
+//              base + r/32 of the lane quarter it uses, so every writer warp fills its own lane
+//              quarter with all rows: thread (quarter q, lane l) stores rows l + 32c in columns
+//              base + c with tcgen05.st (4 scale bytes per row and MMA for NVFP4
+//              scale_vec::4X; one byte per MMA, picked by the scale-factor id, for MXFP8
+//              scale_vec::1X), then signals the stage's `sf_ready` barrier. After the main
+//              loop: tcgen05.ld of the accumulator lanes 32q..32q+31, x alpha, store.
+//   warp 5     TMEM allocator and MMA issuer (one lane): waits `sf_ready`, issues the stage's 4
+//              block-scaled tcgen05.mma, and tcgen05.commit frees the stage (`empty`).
+// A 4-stage shared-memory ring; the tensor pipe sees only MMAs (no tensor-memory copies).
+// Every wait is bounded: on timeout the kernel raises the library's device error word,
+// commits outstanding MMAs before freeing tensor memory, and drains its own copies.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstring>
@@ -33,8 +39,9 @@ __device__ unsigned int g_device_error;      // bit 0: a bounded wait timed out
 namespace {
 
 constexpr int kStages = 4;
+
 constexpr int kBM = 128, kBN = 256, kBKBytes = 128;
-constexpr int kThreads = 256;
+constexpr int kThreads = 192;
 constexpr uint64_t kTimeoutNs = 1500000000ull;     // 1.5 s
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;                   // accumulator columns [0, 256)
@@ -42,25 +49,26 @@ constexpr uint32_t kSfCol = 256;                  // scale-factor columns follow
 
 template <int kKind> struct Cfg;
 template <> struct Cfg<0> {   // NVFP4: K = 256 values (128 B) per stage, 4 MMAs of K = 64
-    static constexpr uint32_t kSfaBytes = 4 * 512, kSfbBytes = 8 * 512;
-    static constexpr uint32_t kSfColsPerStage = 48;   // SFA 4 x 4 + SFB 4 x 8
+    static constexpr uint32_t kSfColsPerStage = 48;   // SFA 4 MMAs x 4 cols + SFB 4 MMAs x 8 cols
+    static constexpr uint32_t kSfRowBytes = 16;       // 16 scales per row and stage
     static constexpr int kValuesPerStage = 256;
 };
 template <> struct Cfg<1> {   // MXFP8: K = 128 values per stage, 4 MMAs of K = 32
-    static constexpr uint32_t kSfaBytes = 512, kSfbBytes = 2 * 512;
-    static constexpr uint32_t kSfColsPerStage = 12;   // SFA 4 + SFB 8 (4 bytes = 4 MMAs)
+    static constexpr uint32_t kSfColsPerStage = 12;   // SFA 4 cols + SFB 8 cols (byte j = MMA j)
+    static constexpr uint32_t kSfRowBytes = 4;        // 4 scales per row and stage
     static constexpr int kValuesPerStage = 128;
 };
 
 constexpr uint32_t kABytes = kBM * kBKBytes;      // 16 KB
 constexpr uint32_t kBBytes = kBN * kBKBytes;      // 32 KB
 
+// stage = A tile, B tile, then the scale staging rows (128 A rows, 256 B rows)
 template <int kKind>
 __host__ __device__ constexpr uint32_t stage_bytes() {
-    return ((kABytes + kBBytes + Cfg<kKind>::kSfaBytes + Cfg<kKind>::kSfbBytes + 1023) / 1024) * 1024;
+    return ((kABytes + kBBytes + (kBM + kBN) * Cfg<kKind>::kSfRowBytes + 1023) / 1024) * 1024;
 }
 template <int kKind>
-__host__ __device__ constexpr uint32_t smem_bytes() { return kStages * stage_bytes<kKind>() + 1024 + 256; }
+__host__ __device__ constexpr uint32_t smem_bytes() { return kStages * stage_bytes<kKind>() + 1024 + 512; }
 
 struct Params {
     CUtensorMap tma_a;
@@ -76,6 +84,8 @@ struct Params {
     int64_t M, N, K;
     int num_kb;
     int n_tiles;
+    int m_tiles;
+    int m_fastest;             // 1: consecutive CTAs walk down M (same B tile)
     int groups;
     int64_t goff[65];
     int gtile[65];
@@ -137,8 +147,23 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  ::"r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(taddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+// cp.async of `bytes` (4 or 16) with zero fill when `valid` is false
+template <int kBytes>
+__device__ __forceinline__ void cp_async_zfill(uint32_t dst, const void* src, bool valid) {
+    if (kBytes == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void mma_nvfp4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                           uint32_t sfa, uint32_t sfb, uint32_t acc) {
@@ -174,10 +199,6 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) |
            (2ull << 61);
 }
-// Descriptor of one 32 x 16-byte scale atom (no swizzle; 8-row groups 128 bytes apart).
-__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (8ull << 32) | (1ull << 46);
-}
 
 // Instruction descriptors (M = 128, N = 256, K-major A and B, dense).
 //   bits 7-9 / 10-12 operand formats, 17-22 N >> 3, 23 scale type (0 UE4M3, 1 UE8M0),
@@ -187,10 +208,6 @@ constexpr uint32_t kIdescNvfp4 = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) 
 constexpr uint32_t kIdescMxfp8 = (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                                  (1u << 23) | ((uint32_t)(kBM >> 4) << 24);
 
-__device__ __forceinline__ uint4 ld_sc16(const uint8_t* p) {
-    return __ldg(reinterpret_cast<const uint4*>(p));
-}
-
 // ------------------------------------------------------------------ the kernel
 template <int kKind>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ Params p) {
@@ -199,7 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     constexpr uint32_t kStage = stage_bytes<kKind>();
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStage);
     uint64_t* empty = full + kStages;
-    uint64_t* accum = empty + kStages;
+
+    uint64_t* sf_ready = empty + kStages;
+    uint64_t* accum = sf_ready + kStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
     int* issued = reinterpret_cast<int*>(tmem_slot + 1);     // stages the producer loaded
     int* consumed = issued + 1;                              // stages the MMA issuer used
@@ -208,18 +227,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
     // ---- tile decode: linear tile -> (group, m0, n0)
     const int t = blockIdx.x;
-    const int mt = t / p.n_tiles, nt = t - mt * p.n_tiles;
+    int mt, nt;
+    if (p.m_fastest) {
+        nt = t / p.m_tiles;
+        mt = t - nt * p.m_tiles;
+    } else {
+        mt = t / p.n_tiles;
+        nt = t - mt * p.n_tiles;
+    }
     int g = 0;
     while (g + 1 < p.groups && p.gtile[g + 1] <= mt) ++g;
     const int64_t m0 = p.goff[g] + (int64_t)(mt - p.gtile[g]) * kBM;
     const int64_t m_end = p.goff[g + 1];
     const int64_t n0 = (int64_t)nt * kBN;
     const int64_t brow0 = (int64_t)g * p.N + n0;
+    constexpr uint32_t kSfRow = Cfg<kKind>::kSfRowBytes;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 3);      // TMA arrive.expect_tx + A-scale + B-scale loaders
-            mbar_init(&empty[s], 1);     // tcgen05.commit
+            mbar_init(&full[s], 1 + 32);  // TMA arrive.expect_tx + 32 producer-lane cp.async arrivals
+            mbar_init(&empty[s], 1);      // tcgen05.commit
+            mbar_init(&sf_ready[s], 4);   // the four scale-writer warps
         }
         mbar_init(accum, 1);
         *issued = 0;
@@ -237,90 +265,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 4) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ producer
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tma_a) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tma_b) : "memory");
-            int kb = 0;
-            for (; kb < p.num_kb; ++kb) {
-                const int s = kb % kStages;
-                const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-                if (!mbar_wait(&empty[s], ph ^ 1u)) break;
-                uint8_t* st = smem + s * kStage;
+        }
+        // scale rows of this lane: A rows m0 + lane + 32q (q < 4), B rows n0 + lane + 32q (q < 8)
+        const uint8_t* bbase =
+            p.b_sc + (p.b_sc_2d ? (int64_t)g * (p.N / 16) * p.sc_ld : (int64_t)g * p.N * p.sc_ld);
+        int kb = 0;
+        for (; kb < p.num_kb; ++kb) {
+            const int s = kb % kStages;
+            const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
+            if (!mbar_wait(&empty[s], ph ^ 1u)) break;
+            uint8_t* st = smem + s * kStage;
+            if (lane == 0) {
                 mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
                 tma_load_2d(&p.tma_a, &full[s], st, kb * kBKBytes, (int32_t)m0);
                 tma_load_2d(&p.tma_b, &full[s], st + kABytes, kb * kBKBytes, (int32_t)brow0);
             }
-            *issued = kb;
-        }
-    } else if (warp == 6 || warp == 7) {
-        // ------------------------------------------------ scale loaders (A: warp 6, B: warp 7)
-        const bool is_b = (warp == 7);
-        constexpr int kMaxR = 8;                       // rows per lane: A 4, B 8
-        const int R = is_b ? 8 : 4;
-        const uint8_t* base;
-        int64_t row_lim;
-        if (!is_b) {
-            base = p.a_sc;
-            row_lim = p.M;
-        } else {
-            base = p.b_sc + (p.b_sc_2d ? (int64_t)g * (p.N / 16) * p.sc_ld : (int64_t)g * p.N * p.sc_ld);
-            row_lim = p.N;
-        }
-        const int64_t r0 = is_b ? n0 : m0;
-        const uint32_t sf_off = kABytes + kBBytes + (is_b ? Cfg<kKind>::kSfaBytes : 0);
-        uint4 cur[kMaxR], nxt[kMaxR];
-        auto load = [&](int kb, uint4 (&dst)[kMaxR]) {
+            const uint32_t stage_sf = smem_u32(st + kABytes + kBBytes);
 #pragma unroll
-            for (int q = 0; q < kMaxR; ++q) {
-                dst[q] = make_uint4(0, 0, 0, 0);
-                if (q < R) {
-                    const int64_t row = r0 + lane + 32 * q;
-                    if (row < row_lim) {
-                        const int64_t srow = (is_b && p.b_sc_2d) ? (row >> 4) : row;
-                        const uint8_t* src = base + srow * p.sc_ld;
-                        if (kKind == 0) {
-                            dst[q] = ld_sc16(src + (int64_t)kb * 16);
-                        } else {
-                            dst[q].x = __ldg(reinterpret_cast<const uint32_t*>(src + (int64_t)kb * 4));
-                        }
-                    }
-                }
+            for (int q = 0; q < 4; ++q) {
+                const int r = lane + 32 * q;
+                const int64_t row = m0 + r;
+                const bool ok = row < p.M;
+                cp_async_zfill<kSfRow>(stage_sf + r * kSfRow,
+                                       p.a_sc + (ok ? row : 0) * p.sc_ld + (int64_t)kb * kSfRow, ok);
             }
-        };
-        load(0, cur);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-            const int s = kb % kStages;
-            const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-            if (kb + 1 < p.num_kb) load(kb + 1, nxt);
-            if (!mbar_wait(&empty[s], ph ^ 1u)) break;
-            uint8_t* sf = smem + s * kStage + sf_off;
-            if (kKind == 0) {
-                // atom (j, h): rows 128h + [0,128) of MMA j; lane l writes rows l, l+32, l+64, l+96
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (h == 1 && !is_b) break;
-                    const uint4 q0 = cur[4 * h], q1 = cur[4 * h + 1], q2 = cur[4 * h + 2], q3 = cur[4 * h + 3];
-                    const int nh = is_b ? 2 : 1;
-                    *reinterpret_cast<uint4*>(sf + (0 * nh + h) * 512 + lane * 16) = make_uint4(q0.x, q1.x, q2.x, q3.x);
-                    *reinterpret_cast<uint4*>(sf + (1 * nh + h) * 512 + lane * 16) = make_uint4(q0.y, q1.y, q2.y, q3.y);
-                    *reinterpret_cast<uint4*>(sf + (2 * nh + h) * 512 + lane * 16) = make_uint4(q0.z, q1.z, q2.z, q3.z);
-                    *reinterpret_cast<uint4*>(sf + (3 * nh + h) * 512 + lane * 16) = make_uint4(q0.w, q1.w, q2.w, q3.w);
-                }
-            } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    if (h == 1 && !is_b) break;
-                    *reinterpret_cast<uint4*>(sf + h * 512 + lane * 16) =
-                        make_uint4(cur[4 * h].x, cur[4 * h + 1].x, cur[4 * h + 2].x, cur[4 * h + 3].x);
-                }
+            for (int q = 0; q < 8; ++q) {
+                const int r = lane + 32 * q;
+                const int64_t row = n0 + r;
+                const bool ok = row < p.N;
+                const int64_t srow = ok ? (p.b_sc_2d ? (row >> 4) : row) : 0;
+                cp_async_zfill<kSfRow>(stage_sf + (kBM + r) * kSfRow, bbase + srow * p.sc_ld + (int64_t)kb * kSfRow, ok);
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[s]);
-#pragma unroll
-            for (int q = 0; q < kMaxR; ++q) cur[q] = nxt[q];
+            cp_async_arrive_noinc(&full[s]);
         }
+        if (lane == 0) *issued = kb;
+        asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -328,30 +312,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (; kb < p.num_kb; ++kb) {
                 const int s = kb % kStages;
                 const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-                if (!mbar_wait(&full[s], ph)) break;
+                if (!mbar_wait(&sf_ready[s], ph)) break;
                 tc_fence_after();
                 const uint32_t sa = smem_u32(smem + s * kStage);
                 const uint32_t sb = sa + kABytes;
-                const uint32_t ssf = sb + kBBytes;
                 const uint32_t sf_col = tmem + kSfCol + (uint32_t)s * Cfg<kKind>::kSfColsPerStage;
                 if (kKind == 0) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) tc_cp_sf(sf_col + 4 * j, desc_sf(ssf + j * 512));
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            tc_cp_sf(sf_col + 16 + 8 * j + 4 * h,
-                                     desc_sf(ssf + Cfg<0>::kSfaBytes + (2 * j + h) * 512));
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         mma_nvfp4(tmem + kAccCol, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
                                   kIdescNvfp4, sf_col + 4 * j, sf_col + 16 + 8 * j,
                                   (kb | j) ? 1u : 0u);
                 } else {
-                    tc_cp_sf(sf_col, desc_sf(ssf));
-                    tc_cp_sf(sf_col + 4, desc_sf(ssf + Cfg<1>::kSfaBytes));
-                    tc_cp_sf(sf_col + 8, desc_sf(ssf + Cfg<1>::kSfaBytes + 512));
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         mma_mxfp8(tmem + kAccCol, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
@@ -367,7 +339,53 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ epilogue warps 0-3
+        // ------------------------------------------------ warps 0-3: scale writers, then epilogue
+        {
+            const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                const int s = kb % kStages;
+                if (!mbar_wait(&full[s], (uint32_t)(kb / kStages) & 1u)) break;
+                tc_fence_after();   // the MMAs that last read this slot's columns have completed
+                const uint8_t* stg = smem + s * kStage + kABytes + kBBytes;
+                const uint32_t sf = tmem + lane_base + kSfCol + (uint32_t)s * Cfg<kKind>::kSfColsPerStage;
+                if (kKind == 0) {
+                    uint4 a[4], b[8];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint4*>(stg + (lane + 32 * c) * 16);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        b[c] = *reinterpret_cast<const uint4*>(stg + (kBM + lane + 32 * c) * 16);
+                    // MMA j: SFA in columns sf + 4j + c, SFB in columns sf + 16 + 8j + c
+                    tmem_st4(sf + 0, a[0].x, a[1].x, a[2].x, a[3].x);
+                    tmem_st4(sf + 4, a[0].y, a[1].y, a[2].y, a[3].y);
+                    tmem_st4(sf + 8, a[0].z, a[1].z, a[2].z, a[3].z);
+                    tmem_st4(sf + 12, a[0].w, a[1].w, a[2].w, a[3].w);
+                    tmem_st4(sf + 16, b[0].x, b[1].x, b[2].x, b[3].x);
+                    tmem_st4(sf + 20, b[4].x, b[5].x, b[6].x, b[7].x);
+                    tmem_st4(sf + 24, b[0].y, b[1].y, b[2].y, b[3].y);
+                    tmem_st4(sf + 28, b[4].y, b[5].y, b[6].y, b[7].y);
+                    tmem_st4(sf + 32, b[0].z, b[1].z, b[2].z, b[3].z);
+                    tmem_st4(sf + 36, b[4].z, b[5].z, b[6].z, b[7].z);
+                    tmem_st4(sf + 40, b[0].w, b[1].w, b[2].w, b[3].w);
+                    tmem_st4(sf + 44, b[4].w, b[5].w, b[6].w, b[7].w);
+                } else {
+                    uint32_t a[4], b[8];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint32_t*>(stg + (lane + 32 * c) * 4);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        b[c] = *reinterpret_cast<const uint32_t*>(stg + (kBM + lane + 32 * c) * 4);
+                    tmem_st4(sf + 0, a[0], a[1], a[2], a[3]);
+                    tmem_st4(sf + 4, b[0], b[1], b[2], b[3]);
+                    tmem_st4(sf + 8, b[4], b[5], b[6], b[7]);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_ready[s]);
+            }
+        }
+        // ------------------------------------------------ epilogue
         const bool ok = mbar_wait(accum, 0);
         tc_fence_after();
         if (ok) {
@@ -496,6 +514,10 @@ cudaError_t launch_kind(const GemmArgs& a, cudaStream_t st) {
     }
     p.goff[a.groups] = a.M;
     p.gtile[a.groups] = (int)tiles_m;
+    p.m_tiles = (int)tiles_m;
+    const double a_bytes = (double)a.M * (double)kbytes, b_bytes = (double)a.N * (double)kbytes;
+    // walk down M (re-reading A from L2) when A is the smaller operand, so B streams once
+    p.m_fastest = (a.groups == 1 && a_bytes < b_bytes) ? 1 : 0;
     const int64_t tiles = tiles_m * p.n_tiles;
     if (tiles <= 0) return cudaSuccess;
     gemm_kernel<kKind><<<(unsigned)tiles, kThreads, smem_bytes<kKind>(), st>>>(p);
