@@ -134,9 +134,6 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
                  " [%0], [%1, {%3, %4}], [%2];"
                  ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y) : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -208,6 +205,180 @@ constexpr uint32_t kIdescNvfp4 = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) 
 constexpr uint32_t kIdescMxfp8 = (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                                  (1u << 23) | ((uint32_t)(kBM >> 4) << 24);
 
+// Epilogue of one 128 x 256 accumulator: warp w (TMEM lane quarter w) loads rows
+// m0 + 32w + lane, 32 columns at a time, scales by alpha and stores fp32 or bf16.
+__device__ __forceinline__ void store_tile(const Params& p, uint32_t tacc, int warp, int lane, int64_t m0,
+                                           int64_t m_end, int64_t n0, float alpha) {
+    const int64_t row = m0 + warp * 32 + lane;
+    const bool row_ok = row < m_end;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tacc + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
+        const int64_t col = n0 + c * 32;
+        if (!row_ok || col >= p.N) continue;
+        const bool full32 = col + 32 <= p.N;
+        if (p.d_bf16) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha),
+                                                          __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
+                pk[i] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + row * p.N + col);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            if (full32) {
+                dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+                dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+            }
+        } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.N + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i >= 4 && !full32) break;
+                dst[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
+                                     __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
+                                     __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
+                                     __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
+            }
+        }
+    }
+}
+
+// Scale writer step (warps 0-3): copy one stage's staged scale rows into tensor memory in the
+// layout the tensor core reads (row r: lane r mod 32 of every lane quarter, column base + r/32).
+// stg: 128 A rows then 256 B rows of kSfRowBytes; sf: this warp's lane quarter, stage columns.
+template <int kKind>
+__device__ __forceinline__ void write_stage_scales(const uint8_t* stg, uint32_t sf, int lane) {
+    if (kKind == 0) {
+        uint4 a[4], b[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint4*>(stg + (lane + 32 * c) * 16);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) b[c] = *reinterpret_cast<const uint4*>(stg + (kBM + lane + 32 * c) * 16);
+        // MMA j: SFA in columns sf + 4j + c, SFB in columns sf + 16 + 8j + c
+        tmem_st4(sf + 0, a[0].x, a[1].x, a[2].x, a[3].x);
+        tmem_st4(sf + 4, a[0].y, a[1].y, a[2].y, a[3].y);
+        tmem_st4(sf + 8, a[0].z, a[1].z, a[2].z, a[3].z);
+        tmem_st4(sf + 12, a[0].w, a[1].w, a[2].w, a[3].w);
+        tmem_st4(sf + 16, b[0].x, b[1].x, b[2].x, b[3].x);
+        tmem_st4(sf + 20, b[4].x, b[5].x, b[6].x, b[7].x);
+        tmem_st4(sf + 24, b[0].y, b[1].y, b[2].y, b[3].y);
+        tmem_st4(sf + 28, b[4].y, b[5].y, b[6].y, b[7].y);
+        tmem_st4(sf + 32, b[0].z, b[1].z, b[2].z, b[3].z);
+        tmem_st4(sf + 36, b[4].z, b[5].z, b[6].z, b[7].z);
+        tmem_st4(sf + 40, b[0].w, b[1].w, b[2].w, b[3].w);
+        tmem_st4(sf + 44, b[4].w, b[5].w, b[6].w, b[7].w);
+    } else {
+        uint32_t a[4], b[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint32_t*>(stg + (lane + 32 * c) * 4);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) b[c] = *reinterpret_cast<const uint32_t*>(stg + (kBM + lane + 32 * c) * 4);
+        tmem_st4(sf + 0, a[0], a[1], a[2], a[3]);
+        tmem_st4(sf + 4, b[0], b[1], b[2], b[3]);
+        tmem_st4(sf + 8, b[4], b[5], b[6], b[7]);
+    }
+}
+
+// cp.async of one stage's scale rows (this lane's 4 A rows and 8 B rows) into staging
+template <int kKind>
+__device__ __forceinline__ void stage_scales(const Params& p, const uint8_t* bbase, int64_t m0, int64_t n0,
+                                             int kb, uint32_t stage_sf, int lane) {
+    constexpr uint32_t kSfRow = Cfg<kKind>::kSfRowBytes;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int r = lane + 32 * q;
+        const int64_t row = m0 + r;
+        const bool ok = row < p.M;
+        cp_async_zfill<kSfRow>(stage_sf + r * kSfRow, p.a_sc + (ok ? row : 0) * p.sc_ld + (int64_t)kb * kSfRow, ok);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int r = lane + 32 * q;
+        const int64_t row = n0 + r;
+        const bool ok = row < p.N;
+        const int64_t srow = ok ? (p.b_sc_2d ? (row >> 4) : row) : 0;
+        cp_async_zfill<kSfRow>(stage_sf + (kBM + r) * kSfRow, bbase + srow * p.sc_ld + (int64_t)kb * kSfRow, ok);
+    }
+}
+
+// ------------------------------------------------------------------ CTA-pair helpers
+#ifndef FP4Q_PAIR_WAIT_SCOPE_CLUSTER
+#define FP4Q_PAIR_WAIT_SCOPE_CLUSTER 0
+#endif
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// shared::cluster address of the same shared variable in the pair's leader (rank 0)
+__device__ __forceinline__ uint32_t leader_addr(const void* p) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(smem_u32(p)));
+    return r;
+}
+// Arrive on a barrier of the pair (default semantics: the tensor-memory writes it publishes are
+// ordered by tcgen05.wait::st + tcgen05.fence::before_thread_sync; a cluster-scope release fence
+// here stalled every writer warp on every stage).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_pair(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+#if FP4Q_PAIR_WAIT_SCOPE_CLUSTER
+    asm volatile("{.reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+#else
+    asm volatile("{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+#endif
+    return ok != 0;
+}
+// bounded wait on a barrier that also receives arrivals from the peer CTA
+__device__ __forceinline__ bool mbar_wait_pair(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait_pair(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_pair(bar, parity)) return true;
+        if ((it & 255u) == 0 && globaltimer() - t0 > kTimeoutNs) {
+            atomicOr(&g_device_error, 1u);
+            return false;
+        }
+    }
+}
+// TMA load into this CTA's shared memory whose completion is counted on a barrier of the pair
+// (here always the leader's)
+__device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, uint32_t bar_cluster_addr, void* dst,
+                                                 int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%3, %4}], [%2];"
+                 ::"r"(smem_u32(dst)), "l"(map), "r"(bar_cluster_addr), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 ::"r"(smem_u32(bar)), "h"((unsigned short)3) : "memory");
+}
+__device__ __forceinline__ void mma2_nvfp4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t sfa, uint32_t sfb, uint32_t acc) {
+    asm volatile("{.reg .pred p; setp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+                 " [%0], %1, %2, %3, [%5], [%6], p;}"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb) : "memory");
+}
+__device__ __forceinline__ void mma2_mxfp8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t sfa, uint32_t sfb, uint32_t acc) {
+    asm volatile("{.reg .pred p; setp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+                 " [%0], %1, %2, %3, [%5], [%6], p;}"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb) : "memory");
+}
+
 // ------------------------------------------------------------------ the kernel
 template <int kKind>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ Params p) {
@@ -241,7 +412,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int64_t m_end = p.goff[g + 1];
     const int64_t n0 = (int64_t)nt * kBN;
     const int64_t brow0 = (int64_t)g * p.N + n0;
-    constexpr uint32_t kSfRow = Cfg<kKind>::kSfRowBytes;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -284,23 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 tma_load_2d(&p.tma_a, &full[s], st, kb * kBKBytes, (int32_t)m0);
                 tma_load_2d(&p.tma_b, &full[s], st + kABytes, kb * kBKBytes, (int32_t)brow0);
             }
-            const uint32_t stage_sf = smem_u32(st + kABytes + kBBytes);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int r = lane + 32 * q;
-                const int64_t row = m0 + r;
-                const bool ok = row < p.M;
-                cp_async_zfill<kSfRow>(stage_sf + r * kSfRow,
-                                       p.a_sc + (ok ? row : 0) * p.sc_ld + (int64_t)kb * kSfRow, ok);
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int r = lane + 32 * q;
-                const int64_t row = n0 + r;
-                const bool ok = row < p.N;
-                const int64_t srow = ok ? (p.b_sc_2d ? (row >> 4) : row) : 0;
-                cp_async_zfill<kSfRow>(stage_sf + (kBM + r) * kSfRow, bbase + srow * p.sc_ld + (int64_t)kb * kSfRow, ok);
-            }
+            stage_scales<kKind>(p, bbase, m0, n0, kb, smem_u32(st + kABytes + kBBytes), lane);
             cp_async_arrive_noinc(&full[s]);
         }
         if (lane == 0) *issued = kb;
@@ -346,39 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const int s = kb % kStages;
                 if (!mbar_wait(&full[s], (uint32_t)(kb / kStages) & 1u)) break;
                 tc_fence_after();   // the MMAs that last read this slot's columns have completed
-                const uint8_t* stg = smem + s * kStage + kABytes + kBBytes;
                 const uint32_t sf = tmem + lane_base + kSfCol + (uint32_t)s * Cfg<kKind>::kSfColsPerStage;
-                if (kKind == 0) {
-                    uint4 a[4], b[8];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint4*>(stg + (lane + 32 * c) * 16);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        b[c] = *reinterpret_cast<const uint4*>(stg + (kBM + lane + 32 * c) * 16);
-                    // MMA j: SFA in columns sf + 4j + c, SFB in columns sf + 16 + 8j + c
-                    tmem_st4(sf + 0, a[0].x, a[1].x, a[2].x, a[3].x);
-                    tmem_st4(sf + 4, a[0].y, a[1].y, a[2].y, a[3].y);
-                    tmem_st4(sf + 8, a[0].z, a[1].z, a[2].z, a[3].z);
-                    tmem_st4(sf + 12, a[0].w, a[1].w, a[2].w, a[3].w);
-                    tmem_st4(sf + 16, b[0].x, b[1].x, b[2].x, b[3].x);
-                    tmem_st4(sf + 20, b[4].x, b[5].x, b[6].x, b[7].x);
-                    tmem_st4(sf + 24, b[0].y, b[1].y, b[2].y, b[3].y);
-                    tmem_st4(sf + 28, b[4].y, b[5].y, b[6].y, b[7].y);
-                    tmem_st4(sf + 32, b[0].z, b[1].z, b[2].z, b[3].z);
-                    tmem_st4(sf + 36, b[4].z, b[5].z, b[6].z, b[7].z);
-                    tmem_st4(sf + 40, b[0].w, b[1].w, b[2].w, b[3].w);
-                    tmem_st4(sf + 44, b[4].w, b[5].w, b[6].w, b[7].w);
-                } else {
-                    uint32_t a[4], b[8];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint32_t*>(stg + (lane + 32 * c) * 4);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        b[c] = *reinterpret_cast<const uint32_t*>(stg + (kBM + lane + 32 * c) * 4);
-                    tmem_st4(sf + 0, a[0], a[1], a[2], a[3]);
-                    tmem_st4(sf + 4, b[0], b[1], b[2], b[3]);
-                    tmem_st4(sf + 8, b[4], b[5], b[6], b[7]);
-                }
+                write_stage_scales<kKind>(smem + s * kStage + kABytes + kBBytes, sf, lane);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -389,44 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const bool ok = mbar_wait(accum, 0);
         tc_fence_after();
         if (ok) {
-            float alpha = 1.0f;
-            if (kKind == 0) alpha = __fmul_rn(p.a_s_dec[0], p.b_s_dec[g]);
-            const int64_t row = m0 + warp * 32 + lane;
-            const bool row_ok = row < m_end;
-#pragma unroll 1
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + kAccCol + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
-                const int64_t col = n0 + c * 32;
-                if (!row_ok || col >= p.N) continue;
-                const bool full32 = col + 32 <= p.N;
-                if (p.d_bf16) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha),
-                                                                  __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
-                        pk[i] = *reinterpret_cast<uint32_t*>(&h2);
-                    }
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + row * p.N + col);
-                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                    if (full32) {
-                        dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-                        dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
-                    }
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.N + col);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        if (i >= 4 && !full32) break;
-                        dst[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
-                                             __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
-                                             __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
-                                             __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
-                    }
-                }
-            }
+            const float alpha = kKind == 0 ? __fmul_rn(p.a_s_dec[0], p.b_s_dec[g]) : 1.0f;
+            store_tile(p, tmem + kAccCol, warp, lane, m0, m_end, n0, alpha);
         }
     }
 
@@ -441,6 +528,171 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (warp == 5) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+
+// ------------------------------------------------------------------ the CTA-pair kernel
+// Two CTAs of a cluster compute one 256 x 256 output tile with tcgen05.mma.cta_group::2
+// (M = 256: each CTA owns 128 rows of A and of the accumulator; each holds 128 of the 256 B
+// rows, so each SM streams half the B tile of the single-CTA kernel: 32 KB instead of 48 KB
+// per stage for the same tensor-core work, and the ring holds 5-6 stages).
+//   producer (warp 4, each CTA): loads its A half and B half; completion is counted on the
+//     leader's `full` barrier (the leader posts the pair's transaction bytes); its lanes also
+//     cp.async this CTA's scale rows into staging (own `sf_full` barrier).
+//   scale writers (warps 0-3, each CTA): write this CTA's A rows and all 256 B rows of scales into
+//     its own tensor memory, then arrive on the leader's `sf_ready` barrier (8 arrivals).
+//   MMA issuer (warp 5 lane 0, leader only): 4 cta_group::2 MMAs per stage; the commit is
+//     multicast to both CTAs' `empty` barriers, and the final one to both `accum` barriers.
+//   epilogue (warps 0-3, each CTA): its own 128 accumulator rows.
+template <int kKind> struct Pair;
+template <> struct Pair<0> { static constexpr int kStages = 5; };
+template <> struct Pair<1> { static constexpr int kStages = 6; };
+constexpr uint32_t kHalfBBytes = 128 * kBKBytes;   // 16 KB
+
+template <int kKind>
+__host__ __device__ constexpr uint32_t pair_stage_bytes() {
+    return ((kABytes + kHalfBBytes + (kBM + kBN) * Cfg<kKind>::kSfRowBytes + 1023) / 1024) * 1024;
+}
+template <int kKind>
+__host__ __device__ constexpr uint32_t pair_smem_bytes() {
+    return Pair<kKind>::kStages * pair_stage_bytes<kKind>() + 1024 + 512;
+}
+constexpr uint32_t kIdesc2Nvfp4 = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                                  (0u << 23) | ((uint32_t)(256 >> 4) << 24);
+constexpr uint32_t kIdesc2Mxfp8 = (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                                  (1u << 23) | ((uint32_t)(256 >> 4) << 24);
+
+template <int kKind>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+gemm_pair_kernel(const __grid_constant__ Params p) {
+    constexpr int S = Pair<kKind>::kStages;
+    constexpr uint32_t kStage = pair_stage_bytes<kKind>();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kStage);   // leader: pair TMA bytes
+    uint64_t* sf_full = full + S;                                        // own: scale staging
+    uint64_t* sf_ready = sf_full + S;                                    // leader: 8 writer warps
+    uint64_t* empty = sf_ready + S;                                      // own: multicast commit
+    uint64_t* accum = empty + S;                                         // own: multicast commit
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+
+    // ---- tile decode: cluster -> (256-row block, n tile); this CTA's rows m0 .. m0 + 127
+    const int c = blockIdx.x >> 1;
+    int mt, nt;
+    if (p.m_fastest) {
+        nt = c / p.m_tiles;
+        mt = c - nt * p.m_tiles;
+    } else {
+        mt = c / p.n_tiles;
+        nt = c - mt * p.n_tiles;
+    }
+    const int64_t m0 = (int64_t)mt * 256 + 128 * (int64_t)rank;
+    const int64_t n0 = (int64_t)nt * kBN;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);        // the leader's arrive.expect_tx (+ both CTAs' bytes)
+            mbar_init(&sf_full[i], 32);    // 32 producer-lane cp.async arrivals
+            mbar_init(&sf_ready[i], 8);    // 4 writer warps x 2 CTAs
+            mbar_init(&empty[i], 1);       // the leader's multicast commit
+        }
+        mbar_init(accum, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ------------------------------------------------ producer (both CTAs)
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tma_a) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tma_b) : "memory");
+        }
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            const int s = kb % S;
+            if (!mbar_wait_pair(&empty[s], ((uint32_t)(kb / S) & 1u) ^ 1u)) break;
+            uint8_t* st = smem + s * kStage;
+            if (lane == 0) {
+                if (leader) mbar_arrive_expect_tx(&full[s], 2 * (kABytes + kHalfBBytes));
+                const uint32_t bar = leader_addr(&full[s]);
+                tma_load_2d_pair(&p.tma_a, bar, st, kb * kBKBytes, (int32_t)m0);
+                tma_load_2d_pair(&p.tma_b, bar, st + kABytes, kb * kBKBytes, (int32_t)(n0 + 128 * rank));
+            }
+            stage_scales<kKind>(p, p.b_sc, m0, n0, kb, smem_u32(st + kABytes + kHalfBBytes), lane);
+            cp_async_arrive_noinc(&sf_full[s]);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp == 5) {
+        // ------------------------------------------------ MMA issuer (leader only)
+        if (leader && lane == 0) {
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                const int s = kb % S;
+                const uint32_t ph = (uint32_t)(kb / S) & 1u;
+                if (!mbar_wait_pair(&full[s], ph) || !mbar_wait_pair(&sf_ready[s], ph)) break;
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + s * kStage);
+                const uint32_t sb = sa + kABytes;
+                const uint32_t sf_col = tmem + kSfCol + (uint32_t)s * Cfg<kKind>::kSfColsPerStage;
+                if (kKind == 0) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma2_nvfp4(tmem + kAccCol, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
+                                   kIdesc2Nvfp4, sf_col + 4 * j, sf_col + 16 + 8 * j, (kb | j) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma2_mxfp8(tmem + kAccCol, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
+                                   kIdesc2Mxfp8 | ((uint32_t)j << 29) | ((uint32_t)j << 4),
+                                   sf_col, sf_col + 4, (kb | j) ? 1u : 0u);
+                }
+                tc_commit_pair(&empty[s]);
+            }
+            // both CTAs' accumulators are complete once every MMA above has finished
+            tc_commit_pair(accum);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ warps 0-3: scale writers, then epilogue
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        const uint32_t ready0 = leader_addr(&sf_ready[0]);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+            const int s = kb % S;
+            if (!mbar_wait(&sf_full[s], (uint32_t)(kb / S) & 1u)) break;
+            tc_fence_after();
+            const uint32_t sf = tmem + lane_base + kSfCol + (uint32_t)s * Cfg<kKind>::kSfColsPerStage;
+            write_stage_scales<kKind>(smem + s * kStage + kABytes + kHalfBBytes, sf, lane);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(ready0 + (uint32_t)s * 8u);
+        }
+        const bool ok = mbar_wait_pair(accum, 0);
+        tc_fence_after();
+        if (ok) {
+            const float alpha = kKind == 0 ? __fmul_rn(p.a_s_dec[0], p.b_s_dec[0]) : 1.0f;
+            store_tile(p, tmem + kAccCol, warp, lane, m0, p.M, n0, alpha);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
     }
 }
 
@@ -524,9 +776,57 @@ cudaError_t launch_kind(const GemmArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// The CTA-pair kernel for one group and M > 128: clusters of 2 CTAs over 256-row blocks.
+template <int kKind>
+cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)pair_smem_bytes<kKind>());
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    Params p;
+    memset(&p, 0, sizeof(p));
+    const uint64_t kbytes = kKind == 0 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
+    if (!make_map(&p.tma_a, a.a, kbytes, (uint64_t)a.M, kBM)) return cudaErrorInvalidValue;
+    if (!make_map(&p.tma_b, a.b, kbytes, (uint64_t)a.N, 128)) return cudaErrorInvalidValue;
+    p.a_sc = a.a_scales;
+    p.b_sc = a.b_scales;
+    p.sc_ld = kKind == 0 ? a.K / 16 : a.K / 32;
+    p.b_sc_2d = (kKind == 0 && a.b_scale_kind == 2) ? 1 : 0;
+    p.a_s_dec = a.a_s_dec;
+    p.b_s_dec = a.b_s_dec;
+    p.d = a.d;
+    p.d_bf16 = a.d_bf16;
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.num_kb = (int)(a.K / Cfg<kKind>::kValuesPerStage);
+    p.n_tiles = (int)((a.N + kBN - 1) / kBN);
+    p.m_tiles = (int)((a.M + 255) / 256);
+    p.groups = 1;
+    const double a_bytes = (double)a.M * (double)kbytes, b_bytes = (double)a.N * (double)kbytes;
+    p.m_fastest = a_bytes < b_bytes ? 1 : 0;
+    const int64_t clusters = (int64_t)p.m_tiles * p.n_tiles;
+    gemm_pair_kernel<kKind><<<(unsigned)(2 * clusters), kThreads, pair_smem_bytes<kKind>(), st>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
+// Kernel choice: the CTA pair for single-group GEMMs with more than one 128-row tile and a main
+// loop of at least 32 stages (it halves each SM's B stream but has a longer per-tile prologue
+// and epilogue); the single-CTA kernel for grouped GEMMs, short K and M <= 128.
+#ifndef FP4Q_GEMM_PAIR
+#define FP4Q_GEMM_PAIR 1
+#endif
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
+    const int64_t stages = a.K / (a.kind == 0 ? Cfg<0>::kValuesPerStage : Cfg<1>::kValuesPerStage);
+    if (FP4Q_GEMM_PAIR && a.groups == 1 && a.M > 128 && stages >= 32)
+        return a.kind == 0 ? launch_pair<0>(a, st) : launch_pair<1>(a, st);
     return a.kind == 0 ? launch_kind<0>(a, st) : launch_kind<1>(a, st);
 }
 

@@ -216,3 +216,54 @@ def test_nvfp4_weight_sweep_largest_sampled(F, orc):
     ref = orc.gemm_nvfp4(xc[idx].cpu().numpy(), xs[idx].cpu().numpy(), 1, float(xsd.item()),
                          wc.cpu().numpy(), ws.cpu().numpy(), 2, float(wsd.item()))
     assert_bf16_rounding_of(yb, ref, "C4 M=16384 sampled")
+
+
+# ------------------------------------------------------------------ CTA-pair kernel (K >= 32 stages)
+@pytest.mark.parametrize("M,N,K", [(300, 272, 4096), (512, 512, 4096), (129, 16, 4096)])
+def test_mxfp8_pair_kernel_random(F, orc, M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    a, asc = rand_mxfp8(rng, M, K)
+    b, bsc = rand_mxfp8(rng, N, K)
+    d = run_mxfp8(F, a, asc, b, bsc)
+    assert_gemm_close(d.cpu().numpy(), orc.gemm_mxfp8(a, asc, b, bsc), f"MXFP8 pair {M}x{N}x{K}")
+
+
+def test_mxfp8_pair_kernel_structured_scales(F, orc):
+    M, N, K = 512, 512, 4096
+    a = np.full((M, K), 0x38, np.uint8)
+    b = np.full((N, K), 0x38, np.uint8)
+    asc = (124 + (np.arange(M)[:, None] % 7) + (np.arange(K // 32)[None, :] % 2)).astype(np.uint8)
+    bsc = (125 + (np.arange(K // 32)[None, :] % 4) + (np.arange(N)[:, None] // 32 % 3)).astype(np.uint8)
+    d = run_mxfp8(F, a, asc, b, bsc, torch.bfloat16)
+    got = d.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert_bf16_rounding_of(got, orc.gemm_mxfp8(a, asc, b, bsc), "MXFP8 pair structured, bf16 out")
+
+
+@pytest.mark.parametrize("M,N,K,two_d", [(300, 272, 8192, False), (256, 256, 8192, True)])
+def test_nvfp4_pair_kernel_random(F, orc, M, N, K, two_d):
+    rng = np.random.default_rng(M * 3 + N + K)
+    a, asc = rand_nvfp4(rng, M, K)
+    b, bsc = rand_nvfp4(rng, N, K, two_d)
+    d = run_nvfp4(F, a, asc, 0.5, b, bsc, 2 if two_d else 1, 0.125)
+    ref = orc.gemm_nvfp4(a, asc, 1, 0.5, b, bsc, 2 if two_d else 1, 0.125)
+    assert_gemm_close(d.cpu().numpy(), ref, f"NVFP4 pair {M}x{N}x{K} 2d={two_d}")
+
+
+def test_mxfp8_dgrad_backward_config_full_size_sampled(F, orc):
+    """Config: dgrad of the backward-requant workload, dX = dY_q W_q^T: M = 8192 tokens,
+    N = K = 4096, fp32 out; 64 sampled rows against the oracle."""
+    M, N, K = 8192, 4096, 4096
+    seed = I.sr_seed(2)
+    dy = I.student_t(M, N, seed=2).cuda()
+    w = I.normal(N, K, seed=23, std=0.02).cuda()
+    wc, ws, wsd, _ = F.quantize_2d(w)
+    g = F.requant_mxfp8(F.IN_BF16, dy, None, None, M, N, 0, 0, 0, F.SR, seed, F.TAG_DY_ROWS)
+    wt = F.requant_mxfp8(F.IN_NVFP4_2D, wc, ws, wsd, N, K, 1, 0, 0, F.SR, seed, F.TAG_WT)
+    dx = F.gemm_mxfp8(g[0], g[1], wt[0], wt[1], torch.float32)
+    torch.cuda.synchronize()
+    assert F.fp4q_device_status() == F.OK
+    rows = np.sort(np.random.default_rng(1).choice(M, 64, replace=False))
+    rows[0], rows[-1] = 0, M - 1
+    idx = torch.from_numpy(rows).cuda()
+    ref = orc.gemm_mxfp8(g[0][idx].cpu().numpy(), g[1][idx].cpu().numpy(), wt[0].cpu().numpy(), wt[1].cpu().numpy())
+    assert_gemm_close(dx[idx].cpu().numpy(), ref, "dgrad 8192x4096x4096 sampled")
