@@ -128,6 +128,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
         }
     }
 }
+#ifndef FP4Q_GEMM_L2_HINTS
+#define FP4Q_GEMM_L2_HINTS 1
+#endif
+// L2 eviction policies for the TMA loads: the operand re-read across the tile sweep is kept
+// (evict_last), the streamed one goes first (evict_first)
+__device__ __forceinline__ uint64_t l2_policy(bool keep) {
+    uint64_t pol;
+    if (keep) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void tma_load_2d_hint(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                                 int32_t x, int32_t y, uint64_t pol) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1, {%3, %4}], [%2], %5;"
+                 ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(pol) : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst,
                                             int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
@@ -360,6 +377,12 @@ __device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, uint32_
                  " [%0], [%1, {%3, %4}], [%2];"
                  ::"r"(smem_u32(dst)), "l"(map), "r"(bar_cluster_addr), "r"(x), "r"(y) : "memory");
 }
+__device__ __forceinline__ void tma_load_2d_pair_hint(const CUtensorMap* map, uint32_t bar_cluster_addr, void* dst,
+                                                      int32_t x, int32_t y, uint64_t pol) {
+    asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1, {%3, %4}], [%2], %5;"
+                 ::"r"(smem_u32(dst)), "l"(map), "r"(bar_cluster_addr), "r"(x), "r"(y), "l"(pol) : "memory");
+}
 __device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
                  ::"r"(smem_u32(bar)), "h"((unsigned short)3) : "memory");
@@ -443,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         // scale rows of this lane: A rows m0 + lane + 32q (q < 4), B rows n0 + lane + 32q (q < 8)
         const uint8_t* bbase =
             p.b_sc + (p.b_sc_2d ? (int64_t)g * (p.N / 16) * p.sc_ld : (int64_t)g * p.N * p.sc_ld);
+        const uint64_t pol_a = l2_policy(p.m_fastest != 0), pol_b = l2_policy(p.m_fastest == 0);
         int kb = 0;
         for (; kb < p.num_kb; ++kb) {
             const int s = kb % kStages;
@@ -451,8 +475,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             uint8_t* st = smem + s * kStage;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
-                tma_load_2d(&p.tma_a, &full[s], st, kb * kBKBytes, (int32_t)m0);
-                tma_load_2d(&p.tma_b, &full[s], st + kABytes, kb * kBKBytes, (int32_t)brow0);
+                if (FP4Q_GEMM_L2_HINTS) {
+                    tma_load_2d_hint(&p.tma_a, &full[s], st, kb * kBKBytes, (int32_t)m0, pol_a);
+                    tma_load_2d_hint(&p.tma_b, &full[s], st + kABytes, kb * kBKBytes, (int32_t)brow0, pol_b);
+                } else {
+                    tma_load_2d(&p.tma_a, &full[s], st, kb * kBKBytes, (int32_t)m0);
+                    tma_load_2d(&p.tma_b, &full[s], st + kABytes, kb * kBKBytes, (int32_t)brow0);
+                }
             }
             stage_scales<kKind>(p, bbase, m0, n0, kb, smem_u32(st + kABytes + kBBytes), lane);
             cp_async_arrive_noinc(&full[s]);
@@ -621,6 +650,7 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tma_a) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tma_b) : "memory");
         }
+        const uint64_t pol_a = l2_policy(p.m_fastest != 0), pol_b = l2_policy(p.m_fastest == 0);
         for (int kb = 0; kb < p.num_kb; ++kb) {
             const int s = kb % S;
             if (!mbar_wait_pair(&empty[s], ((uint32_t)(kb / S) & 1u) ^ 1u)) break;
@@ -628,8 +658,13 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
             if (lane == 0) {
                 if (leader) mbar_arrive_expect_tx(&full[s], 2 * (kABytes + kHalfBBytes));
                 const uint32_t bar = leader_addr(&full[s]);
-                tma_load_2d_pair(&p.tma_a, bar, st, kb * kBKBytes, (int32_t)m0);
-                tma_load_2d_pair(&p.tma_b, bar, st + kABytes, kb * kBKBytes, (int32_t)(n0 + 128 * rank));
+                if (FP4Q_GEMM_L2_HINTS) {
+                    tma_load_2d_pair_hint(&p.tma_a, bar, st, kb * kBKBytes, (int32_t)m0, pol_a);
+                    tma_load_2d_pair_hint(&p.tma_b, bar, st + kABytes, kb * kBKBytes, (int32_t)(n0 + 128 * rank), pol_b);
+                } else {
+                    tma_load_2d_pair(&p.tma_a, bar, st, kb * kBKBytes, (int32_t)m0);
+                    tma_load_2d_pair(&p.tma_b, bar, st + kABytes, kb * kBKBytes, (int32_t)(n0 + 128 * rank));
+                }
             }
             stage_scales<kKind>(p, p.b_sc, m0, n0, kb, smem_u32(st + kABytes + kHalfBBytes), lane);
             cp_async_arrive_noinc(&sf_full[s]);
