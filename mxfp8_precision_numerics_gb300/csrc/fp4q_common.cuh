@@ -120,6 +120,83 @@ __device__ __forceinline__ uint32_t e4m3_sr(float t, uint32_t r16) {
 }
 
 // ---------------------------------------------------------------------------------------
+// The same stochastic rounding done by the conversion unit, two values per instruction.
+// cvt.rs.satfinite.e4m3x4.f32 packs four results; the result in byte 0 (fourth source
+// operand) is rounded up exactly when F + (rbits[15:0] << 4) carries, the one in byte 2
+// (second operand) likewise with rbits[31:16] -- the rule of e4m3_sr with r16 taken from
+// those halves, including the subnormal range and saturation to 448. Bytes 1 and 3 draw on
+// the same halves bit-reversed, so they would not be independent draws: they are fed zero.
+// A device test checks this against the oracle's rounding on every grid point, midpoint
+// and a million random (value, bits) pairs.
+// Returns byte 0 = even, byte 2 = odd (bytes 1, 3 zero).
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3x2_sr_hw(float even, float odd, uint32_t rbits) {
+    uint32_t d;
+    asm("cvt.rs.satfinite.e4m3x4.f32 %0, {%1, %2, %1, %3}, %4;"
+        : "=r"(d) : "f"(0.0f), "f"(odd), "f"(even), "r"(rbits));
+    return d;
+}
+
+// Four E4M3 codes, round to nearest even with saturation, byte k = code of the k-th
+// argument (hardware conversion; first operand of each x2 instruction -> high byte).
+__device__ __forceinline__ uint32_t e4m3x4_rn_hw(float a, float b, float c, float e) {
+    uint32_t d;
+    asm("{.reg .b16 l, h;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n\t"
+        "mov.b32 %0, {l, h};}"
+        : "=r"(d) : "f"(a), "f"(b), "f"(c), "f"(e));
+    return d;
+}
+
+// Two packed E2M1 codes (low nibble = first value) -> f16x2 (low half = first value).
+// Every E2M1 value is exact in f16.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+    uint32_t h;
+    asm("{.reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t;}" : "=r"(h) : "r"(byte));
+    return h;
+}
+
+// Eight packed E2M1 codes times one E4M3 block scale times the fp32 tensor scale:
+// out[j] = (E2M1(code_j) * scale) * s_dec. The first product is formed in f16x2 and is
+// exact there (at most 2 x 4 significant bits, magnitudes in [2^-10, 2688]), so the only
+// rounding is the fp32 multiply by s_dec, as in the definition.
+// sc2 = the block scale as f16 in both halves.
+__device__ __forceinline__ void dequant8_f16(uint32_t word, uint32_t sc2, float s_dec, float* out) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        uint32_t h = e2m1x2_to_f16x2(word >> (8 * b));
+        asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h) : "r"(sc2));
+        float lo, hi;
+        asm("{.reg .f16 l, h; mov.b32 {l, h}, %2; cvt.f32.f16 %0, l; cvt.f32.f16 %1, h;}"
+            : "=f"(lo), "=f"(hi) : "r"(h));
+        out[2 * b] = __fmul_rn(lo, s_dec);
+        out[2 * b + 1] = __fmul_rn(hi, s_dec);
+    }
+}
+
+// An E4M3 scale byte as f16 in both halves of a word (exact: E4M3 values are f16 values).
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_dup(uint32_t c) {
+    uint32_t h;
+    asm("{.reg .f16 s; cvt.rn.f16.f32 s, %1; mov.b32 %0, {s, s};}" : "=r"(h) : "f"(e4m3_to_f32(c)));
+    return h;
+}
+
+// Sign flips of the random Hadamard transform applied to packed inputs: negation is exact,
+// so flipping the source is the same as flipping the dequantized value.
+// Nibble mask for eight E2M1 codes at transform positions p0 .. p0+7.
+__device__ __forceinline__ uint32_t e2m1_sign_mask8(uint32_t signs, int p0) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m |= ((signs >> (p0 + j)) & 1u) << (4 * j + 3);
+    return m;
+}
+// Mask for two bf16 values (one 32-bit word) at transform positions p, p+1.
+__device__ __forceinline__ uint32_t bf16_sign_mask2(uint32_t signs, int p) {
+    return (((signs >> p) & 1u) << 15) | (((signs >> (p + 1)) & 1u) << 31);
+}
+
+// ---------------------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
 // SC'11): ten rounds of two 32x32->64 multiplies with the Weyl key schedule.
 // ---------------------------------------------------------------------------------------
@@ -151,10 +228,8 @@ __device__ __forceinline__ uint32_t slice16(uint4 w, int j) {
 // distances 1, 2, 4, 8 (Sylvester H16 = H2 (x) H8), then the exact scaling by 1/4.
 // ("Pretraining Large Language Models with NVFP4", "Random Hadamard Transforms".)
 // ---------------------------------------------------------------------------------------
-__device__ __forceinline__ void rht16_inplace(float* v, uint32_t signs) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        if ((signs >> i) & 1u) v[i] = -v[i];
+// fwht16_quarter is the same without the sign step, for inputs already sign-flipped.
+__device__ __forceinline__ void fwht16_quarter(float* v) {
 #pragma unroll
     for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll
@@ -168,6 +243,13 @@ __device__ __forceinline__ void rht16_inplace(float* v, uint32_t signs) {
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+}
+
+__device__ __forceinline__ void rht16_inplace(float* v, uint32_t signs) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if ((signs >> i) & 1u) v[i] = -v[i];
+    fwht16_quarter(v);
 }
 
 }  // namespace fp4q

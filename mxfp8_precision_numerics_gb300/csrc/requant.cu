@@ -22,14 +22,15 @@
 namespace fp4q {
 
 // Quantize 32 fp32 values (one MXFP8 block) and store 32 E4M3 bytes + 1 E8M0 byte.
+// kRht: the block is two transform groups whose sign flips the caller has already applied;
+// the butterflies and the 1/4 scaling happen here.
 template <bool kRht, bool kSR>
-__device__ __forceinline__ void mx_encode_block(float (&v)[32], uint32_t signs, uint64_t seed,
-                                                uint32_t tag, uint64_t out_idx0,
-                                                uint8_t* __restrict__ out32,
+__device__ __forceinline__ void mx_encode_block(float (&v)[32], uint64_t seed, uint32_t tag,
+                                                uint64_t out_idx0, uint8_t* __restrict__ out32,
                                                 uint8_t* __restrict__ out_sc) {
     if (kRht) {
-        rht16_inplace(v, signs);
-        rht16_inplace(v + 16, signs);
+        fwht16_quarter(v);
+        fwht16_quarter(v + 16);
     }
     float amax = 0.0f;
 #pragma unroll
@@ -39,17 +40,18 @@ __device__ __forceinline__ void mx_encode_block(float (&v)[32], uint32_t signs, 
     uint32_t words[8];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-        uint4 r = make_uint4(0, 0, 0, 0);
-        if (kSR) r = sr_block8(seed, tag, (out_idx0 >> 3) + (uint64_t)g);
-        uint32_t w0 = 0, w1 = 0;
+        float t[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float t = __fmul_rn(v[8 * g + j], inv);
-            uint32_t c = kSR ? e4m3_sr(t, slice16(r, j)) : e4m3_rne_sat(t);
-            if (j < 4) w0 |= c << (8 * j); else w1 |= c << (8 * (j - 4));
+        for (int j = 0; j < 8; ++j) t[j] = __fmul_rn(v[8 * g + j], inv);
+        if (kSR) {
+            // element 8g+j draws the low (j even) or high (j odd) half of word j/2
+            const uint4 r = sr_block8(seed, tag, (out_idx0 >> 3) + (uint64_t)g);
+            words[2 * g] = __byte_perm(e4m3x2_sr_hw(t[0], t[1], r.x), e4m3x2_sr_hw(t[2], t[3], r.y), 0x6420);
+            words[2 * g + 1] = __byte_perm(e4m3x2_sr_hw(t[4], t[5], r.z), e4m3x2_sr_hw(t[6], t[7], r.w), 0x6420);
+        } else {
+            words[2 * g] = e4m3x4_rn_hw(t[0], t[1], t[2], t[3]);
+            words[2 * g + 1] = e4m3x4_rn_hw(t[4], t[5], t[6], t[7]);
         }
-        words[2 * g] = w0;
-        words[2 * g + 1] = w1;
     }
     uint4* o = reinterpret_cast<uint4*>(out32);
     __stcs(o, make_uint4(words[0], words[1], words[2], words[3]));
@@ -57,14 +59,10 @@ __device__ __forceinline__ void mx_encode_block(float (&v)[32], uint32_t signs, 
     *out_sc = (uint8_t)(e + 127);
 }
 
-// Dequantize 8 packed E2M1 codes (one 32-bit word) with block scale * s_dec into fp32:
-// value = (E2M1(code) * E4M3(scale)) * s_dec, the first product exact.
-__device__ __forceinline__ void dequant8(uint32_t word, float sc, float s_dec, float* out) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        float c = e2m1_to_f32((word >> (4 * j)) & 15u);
-        out[j] = __fmul_rn(__fmul_rn(c, sc), s_dec);
-    }
+// Two bf16 values of one 32-bit word -> fp32 (exact).
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float* out) {
+    out[0] = bf16_to_f32(w & 0xFFFFu);
+    out[1] = __uint_as_float(w & 0xFFFF0000u);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -75,6 +73,14 @@ __global__ void __launch_bounds__(256) requant_rows_kernel(RequantArgs a) {
     const int64_t nb = a.cols >> 5;
     const int64_t total = a.rows * nb;
     const float s_dec = (kKind == 0) ? 1.0f : *a.in_s_dec;
+    // sign masks of the transform positions, packed like the input words
+    uint32_t bm[8], nm0 = 0, nm1 = 0;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) bm[p] = kRht ? bf16_sign_mask2(a.rht_signs, 2 * p) : 0u;
+    if (kRht) {
+        nm0 = e2m1_sign_mask8(a.rht_signs, 0);
+        nm1 = e2m1_sign_mask8(a.rht_signs, 8);
+    }
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < total; b += stride) {
         const int64_t r = b / nb, j = b - r * nb;
@@ -87,10 +93,7 @@ __global__ void __launch_bounds__(256) requant_rows_kernel(RequantArgs a) {
                 uint4 p = __ldcs(src + q);
                 uint32_t w[4] = {p.x, p.y, p.z, p.w};
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    v[8 * q + 2 * k] = bf16_to_f32(w[k] & 0xFFFFu);
-                    v[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-                }
+                for (int k = 0; k < 4; ++k) bf16x2_to_f32(w[k] ^ bm[4 * (q & 1) + k], v + 8 * q + 2 * k);
             }
         } else {
             const uint4 c = __ldcs(reinterpret_cast<const uint4*>(
@@ -103,19 +106,21 @@ __global__ void __launch_bounds__(256) requant_rows_kernel(RequantArgs a) {
                 s0 = a.in_scales[(r >> 4) * (a.cols >> 4) + 2 * j];
                 s1 = a.in_scales[(r >> 4) * (a.cols >> 4) + 2 * j + 1];
             }
-            const float f0 = e4m3_to_f32(s0), f1 = e4m3_to_f32(s1);
-            dequant8(c.x, f0, s_dec, v);
-            dequant8(c.y, f0, s_dec, v + 8);
-            dequant8(c.z, f1, s_dec, v + 16);
-            dequant8(c.w, f1, s_dec, v + 24);
+            const uint32_t f0 = e4m3_to_f16x2_dup(s0), f1 = e4m3_to_f16x2_dup(s1);
+            dequant8_f16(c.x ^ nm0, f0, s_dec, v);
+            dequant8_f16(c.y ^ nm1, f0, s_dec, v + 8);
+            dequant8_f16(c.z ^ nm0, f1, s_dec, v + 16);
+            dequant8_f16(c.w ^ nm1, f1, s_dec, v + 24);
         }
-        mx_encode_block<kRht, kSR>(v, a.rht_signs, a.seed, a.tag, (uint64_t)(r * a.cols + j * 32),
+        mx_encode_block<kRht, kSR>(v, a.seed, a.tag, (uint64_t)(r * a.cols + j * 32),
                                    a.out_e4m3 + r * a.cols + j * 32, a.out_e8m0 + b);
     }
 }
 
 // ---------------------------------------------------------------------------------------
-// transpose = 1: 64 x 64 input tile per CTA, 128 threads.
+// transpose = 1: 64 x 64 input tile per CTA, 128 threads. The transform groups run along
+// the input's rows (the output's contiguous dimension), so the sign of input row r is
+// that of position r mod 16 and is applied to whole packed words at load time.
 // ---------------------------------------------------------------------------------------
 constexpr int kTR = 64, kTC = 64, kPad = 1;
 
@@ -135,13 +140,12 @@ __global__ void __launch_bounds__(128) requant_t_kernel(RequantArgs a) {
             const int rr = v >> 3, cc = (v & 7) * 8;
             float* dst = &tile[rr][cc];
             if (r0 + rr < a.rows && c0 + cc < a.cols) {
+                const uint32_t m = kRht ? ((a.rht_signs >> (rr & 15)) & 1u) * 0x80008000u : 0u;
                 uint4 p = __ldcs(reinterpret_cast<const uint4*>(in + (r0 + rr) * a.cols + c0 + cc));
-                uint32_t w[4] = {p.x, p.y, p.z, p.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    dst[2 * k] = bf16_to_f32(w[k] & 0xFFFFu);
-                    dst[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-                }
+                bf16x2_to_f32(p.x ^ m, dst);
+                bf16x2_to_f32(p.y ^ m, dst + 2);
+                bf16x2_to_f32(p.z ^ m, dst + 4);
+                bf16x2_to_f32(p.w ^ m, dst + 6);
             }
         }
     } else {
@@ -149,6 +153,7 @@ __global__ void __launch_bounds__(128) requant_t_kernel(RequantArgs a) {
         const int64_t gr = r0 + rr, gc = c0 + 32 * half;
         if (gr < a.rows && gc < a.cols) {
             const float s_dec = *a.in_s_dec;
+            const uint32_t m = kRht ? ((a.rht_signs >> (rr & 15)) & 1u) * 0x88888888u : 0u;
             const uint4 c = __ldcs(reinterpret_cast<const uint4*>(
                 static_cast<const uint8_t*>(a.in) + gr * (a.cols >> 1) + (gc >> 1)));
             uint32_t s0, s1;
@@ -159,12 +164,12 @@ __global__ void __launch_bounds__(128) requant_t_kernel(RequantArgs a) {
                 s0 = a.in_scales[(gr >> 4) * (a.cols >> 4) + (gc >> 4)];
                 s1 = a.in_scales[(gr >> 4) * (a.cols >> 4) + (gc >> 4) + 1];
             }
-            const float f0 = e4m3_to_f32(s0), f1 = e4m3_to_f32(s1);
+            const uint32_t f0 = e4m3_to_f16x2_dup(s0), f1 = e4m3_to_f16x2_dup(s1);
             float* dst = &tile[rr][32 * half];
-            dequant8(c.x, f0, s_dec, dst);
-            dequant8(c.y, f0, s_dec, dst + 8);
-            dequant8(c.z, f1, s_dec, dst + 16);
-            dequant8(c.w, f1, s_dec, dst + 24);
+            dequant8_f16(c.x ^ m, f0, s_dec, dst);
+            dequant8_f16(c.y ^ m, f0, s_dec, dst + 8);
+            dequant8_f16(c.z ^ m, f1, s_dec, dst + 16);
+            dequant8_f16(c.w ^ m, f1, s_dec, dst + 24);
         }
     }
     __syncthreads();
@@ -177,7 +182,7 @@ __global__ void __launch_bounds__(128) requant_t_kernel(RequantArgs a) {
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = tile[32 * blk + k][c];
         const int64_t oidx = orow * a.rows + ocol;
-        mx_encode_block<kRht, kSR>(v, a.rht_signs, a.seed, a.tag, (uint64_t)oidx,
+        mx_encode_block<kRht, kSR>(v, a.seed, a.tag, (uint64_t)oidx,
                                    a.out_e4m3 + oidx, a.out_e8m0 + (oidx >> 5));
     }
 }

@@ -1,5 +1,6 @@
 // cvt_probe.cu — test-only kernels that exercise device building blocks of the library in
-// isolation: the E2M1 / E4M3 encoders against the hardware conversion instructions, and
+// isolation: the E2M1 / E4M3 encoders against the hardware conversion instructions, the
+// hardware stochastic rounding and the f16x2 dequantization path, and
 // the Philox4x32-10 generator against cuRAND's implementation of the same published
 // generator. Every kernel is one thread per element with a bounds check; nothing waits.
 #include <cstdint>
@@ -35,6 +36,27 @@ __global__ void e4m3_sr_kernel(const float* in, const uint32_t* r16, uint8_t* ou
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     out[i] = (uint8_t)fp4q::e4m3_sr(in[i], r16[i]);
+}
+
+// Hardware stochastic rounding of (even, odd) pairs with one random word per pair: the
+// whole 32-bit result is returned so that the test also sees the unused bytes.
+__global__ void e4m3x2_sr_hw_kernel(const float* in, const uint32_t* rbits, uint32_t* out, int n) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    out[i] = fp4q::e4m3x2_sr_hw(in[2 * i], in[2 * i + 1], rbits[i]);
+}
+
+// Dequantization of eight packed E2M1 codes with one E4M3 block scale and an fp32 tensor
+// scale, through the f16x2 conversion path (f16) and the plain fp32 decode (ref).
+__global__ void dequant8_kernel(const uint32_t* words, const uint8_t* scales, float s_dec, float* f16,
+                                float* ref, int n) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const uint32_t w = words[i], sc = scales[i];
+    fp4q::dequant8_f16(w, fp4q::e4m3_to_f16x2_dup(sc), s_dec, f16 + 8 * i);
+    const float scf = fp4q::e4m3_to_f32(sc);
+    for (int j = 0; j < 8; ++j)
+        ref[8 * i + j] = __fmul_rn(__fmul_rn(fp4q::e2m1_to_f32((w >> (4 * j)) & 15u), scf), s_dec);
 }
 
 __global__ void philox_kernel(const uint32_t* ctr, const uint32_t* key, uint32_t* mine,
@@ -79,6 +101,21 @@ __attribute__((visibility("default"))) int probe_e4m3_sr(const float* in, const 
                                                           int n, cudaStream_t st) {
     if (n <= 0) return 0;
     e4m3_sr_kernel<<<blocks(n), 256, 0, st>>>(in, r16, out, n);
+    return (int)cudaGetLastError();
+}
+
+__attribute__((visibility("default"))) int probe_e4m3x2_sr_hw(const float* in, const uint32_t* rbits,
+                                                              uint32_t* out, int n, cudaStream_t st) {
+    if (n <= 0) return 0;
+    e4m3x2_sr_hw_kernel<<<blocks(n), 256, 0, st>>>(in, rbits, out, n);
+    return (int)cudaGetLastError();
+}
+
+__attribute__((visibility("default"))) int probe_dequant8(const uint32_t* words, const uint8_t* scales,
+                                                          float s_dec, float* f16, float* ref, int n,
+                                                          cudaStream_t st) {
+    if (n <= 0) return 0;
+    dequant8_kernel<<<blocks(n), 256, 0, st>>>(words, scales, s_dec, f16, ref, n);
     return (int)cudaGetLastError();
 }
 

@@ -151,3 +151,55 @@ def test_philox_matches_oracle_and_curand(P, orc):
     for i in range(0, n, 97):
         assert np.array_equal(mine[i], orc.philox4x32_10(ctr[i], key[i]))
     assert list(mine[0]) == [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]
+
+
+def test_e4m3_hardware_sr_pairs_match_oracle(P, orc):
+    """The conversion unit's stochastic rounding, as the requant kernels use it: value pair
+    (even, odd) with one random word, even rounded with its low half, odd with its high half,
+    the two other result bytes zero. Grid points, midpoints, the subnormal range, 448."""
+    rng = np.random.default_rng(4)
+    x = e4m3_inputs(rng)
+    x = x[np.abs(x) <= 448.0]
+    x = rng.permutation(x)
+    x = x[: len(x) // 2 * 2]
+    n = len(x) // 2
+    rb = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+    rb[:40] = [0, 0xFFFFFFFF, 0x0000FFFF, 0xFFFF0000, 0x80008000, 0x00010001, 0xFFFEFFFE, 0x7FFF8000] * 5
+    xd = torch.from_numpy(x).cuda()
+    rd = torch.from_numpy(rb.view(np.int32)).cuda()
+    out = torch.empty(n, dtype=torch.int32, device="cuda")
+    assert P.probe_e4m3x2_sr_hw(_p(xd), _p(rd), _p(out), n, _stream()) == 0
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().view(np.uint32)
+    lib = orc.lib()
+    sr = lib.orc_e4m3_encode_sr
+    want_even = np.fromiter((sr(float(v), int(k) & 0xFFFF) for v, k in zip(x[0::2], rb)), np.uint32, count=n)
+    want_odd = np.fromiter((sr(float(v), int(k) >> 16) for v, k in zip(x[1::2], rb)), np.uint32, count=n)
+    assert_bytes_equal((got & 0xFF).astype(np.uint8), want_even.astype(np.uint8), "hw SR byte 0 (even)")
+    assert_bytes_equal(((got >> 16) & 0xFF).astype(np.uint8), want_odd.astype(np.uint8), "hw SR byte 2 (odd)")
+    assert not np.any(got & 0xFF00FF00), "hw SR: unused result bytes not zero"
+
+
+@pytest.mark.parametrize("s_dec", [1.0, 0.0123456789, 3.0e-30, 7.5e20])
+def test_dequant8_f16_path_matches_oracle(P, orc, s_dec):
+    """E2M1 x E4M3 x fp32 through the f16x2 conversion path equals the definition
+    (exact product of the two decoded values, then one fp32 rounding), signed zeros included."""
+    rng = np.random.default_rng(5)
+    scales = np.array([c for c in range(256) if (c & 0x7F) != 0x7F] * 16, dtype=np.uint8)
+    n = len(scales)
+    words = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+    words[:2] = [0x76543210, 0xFEDCBA98]          # every code once
+    wd = torch.from_numpy(words.view(np.int32)).cuda()
+    sd = torch.from_numpy(scales).cuda()
+    f16 = torch.empty(8 * n, dtype=torch.float32, device="cuda")
+    ref = torch.empty_like(f16)
+    assert P.probe_dequant8(_p(wd), _p(sd), ctypes.c_float(s_dec), _p(f16), _p(ref), n, _stream()) == 0
+    torch.cuda.synchronize()
+    e2 = np.array([orc.e2m1_decode(c) for c in range(16)], dtype=np.float64)
+    e4 = np.array([orc.e4m3_decode(c) if (c & 0x7F) != 0x7F else 0.0 for c in range(256)], dtype=np.float64)
+    codes = (words[:, None] >> (4 * np.arange(8, dtype=np.uint32))) & 15
+    prod = e2[codes] * e4[scales][:, None]                # exact in fp64
+    want = (prod.astype(np.float32) * np.float32(s_dec)).astype(np.float32).reshape(-1)
+    got = f16.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), "f16x2 dequant differs from the definition"
+    assert np.array_equal(got.view(np.uint32), ref.cpu().numpy().view(np.uint32))
