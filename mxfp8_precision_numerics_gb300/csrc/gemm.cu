@@ -73,6 +73,8 @@ __host__ __device__ constexpr uint32_t smem_bytes() { return kStages * stage_byt
 struct Params {
     CUtensorMap tma_a;
     CUtensorMap tma_b;
+    CUtensorMap tma_sfa;       // pair kernel: scale rows of A, box {16 B, 128 rows}
+    CUtensorMap tma_sfb;       // pair kernel: scale rows of B, box {16 B, 256 rows (16 for 2D tiles)}
     const uint8_t* a_sc;
     const uint8_t* b_sc;
     int64_t sc_ld;             // scale bytes per row (K/16 NVFP4, K/32 MXFP8)
@@ -371,12 +373,6 @@ __device__ __forceinline__ bool mbar_wait_pair(uint64_t* bar, uint32_t parity) {
 }
 // TMA load into this CTA's shared memory whose completion is counted on a barrier of the pair
 // (here always the leader's)
-__device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, uint32_t bar_cluster_addr, void* dst,
-                                                 int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%3, %4}], [%2];"
-                 ::"r"(smem_u32(dst)), "l"(map), "r"(bar_cluster_addr), "r"(x), "r"(y) : "memory");
-}
 __device__ __forceinline__ void tma_load_2d_pair_hint(const CUtensorMap* map, uint32_t bar_cluster_addr, void* dst,
                                                       int32_t x, int32_t y, uint64_t pol) {
     asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
@@ -574,36 +570,97 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 //   MMA issuer (warp 5 lane 0, leader only): 4 cta_group::2 MMAs per stage; the commit is
 //     multicast to both CTAs' `empty` barriers, and the final one to both `accum` barriers.
 //   epilogue (warps 0-3, each CTA): its own 128 accumulator rows.
+// Pipeline depths of the pair kernel.
+//   S   A/B stages in shared memory (TMA, counted on the leader's `full` barrier)
+//   G   K-blocks per scale unit: one TMA box 16 bytes wide per operand holds the scales of
+//       G K-blocks for every row of the tile (4 x 4 E8M0 for MXFP8, 16 E4M3 for NVFP4)
+//   R   scale units staged in shared memory
+//   DU  how many units the scale loads run ahead of the A/B loads
+//   T   scale slots in tensor memory (written by warps 0-3, read by the MMAs)
+// Scales travel by TMA (async proxy, no load/store-unit traffic: per-row 4-byte copies
+// through L1 took most of the shared-memory bandwidth the tensor core needs), their loads
+// run DU units ahead of the A/B loads and the writers may fill up to T tensor-memory slots
+// ahead of the MMAs. Tensor memory: 256 accumulator columns + T x kSfColsPerStage <= 512.
 template <int kKind> struct Pair;
-template <> struct Pair<0> { static constexpr int kStages = 5; };
-template <> struct Pair<1> { static constexpr int kStages = 6; };
+template <> struct Pair<0> { static constexpr int S = 5, G = 1, R = 6, DU = 3, T = 5; };
+template <> struct Pair<1> { static constexpr int S = 6, G = 4, R = 3, DU = 2, T = 16; };
+static_assert(256 + Pair<0>::T * Cfg<0>::kSfColsPerStage <= kTmemCols, "NVFP4 scale slots");
+static_assert(256 + Pair<1>::T * Cfg<1>::kSfColsPerStage <= kTmemCols, "MXFP8 scale slots");
+static_assert(Pair<0>::R >= Pair<0>::DU + 1 && Pair<1>::R >= Pair<1>::DU + 1, "scale ring depth");
 constexpr uint32_t kHalfBBytes = 128 * kBKBytes;   // 16 KB
+constexpr uint32_t kPairStage = kABytes + kHalfBBytes;   // 32 KB, 1024-aligned
+constexpr uint32_t kSfUnitA = kBM * 16;            // 2 KB: 128 A rows x 16 B
+constexpr uint32_t kSfUnitB = kBN * 16;            // 4 KB: 256 B rows x 16 B (2D tiles: 16 rows used)
+constexpr uint32_t kSfUnit = kSfUnitA + kSfUnitB;
 
 template <int kKind>
-__host__ __device__ constexpr uint32_t pair_stage_bytes() {
-    return ((kABytes + kHalfBBytes + (kBM + kBN) * Cfg<kKind>::kSfRowBytes + 1023) / 1024) * 1024;
-}
-template <int kKind>
 __host__ __device__ constexpr uint32_t pair_smem_bytes() {
-    return Pair<kKind>::kStages * pair_stage_bytes<kKind>() + 1024 + 512;
+    return Pair<kKind>::S * kPairStage + Pair<kKind>::R * kSfUnit + 1024 + 1024;
 }
+static_assert(pair_smem_bytes<0>() <= 227 * 1024, "NVFP4 pair shared memory");
+static_assert(pair_smem_bytes<1>() <= 227 * 1024, "MXFP8 pair shared memory");
 constexpr uint32_t kIdesc2Nvfp4 = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                                   (0u << 23) | ((uint32_t)(256 >> 4) << 24);
 constexpr uint32_t kIdesc2Mxfp8 = (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                                   (1u << 23) | ((uint32_t)(256 >> 4) << 24);
 
+// Scale writer step of the pair kernel: K-block `sub` of a staged unit (rows 16 B apart) into
+// tensor memory, in the layout the tensor core reads (row r: lane r mod 32 of every lane
+// quarter, column base + r/32). b2d: B holds one scale row per 16 rows (16 x 16 tiles).
+template <int kKind>
+__device__ __forceinline__ void write_unit_scales(const uint8_t* unit, int sub, bool b2d, uint32_t sf, int lane) {
+    const uint8_t* ua = unit;
+    const uint8_t* ub = unit + kSfUnitA;
+    if (kKind == 0) {
+        uint4 a[4], b[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint4*>(ua + (lane + 32 * c) * 16);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int r = lane + 32 * c;
+            b[c] = *reinterpret_cast<const uint4*>(ub + (b2d ? (r >> 4) : r) * 16);
+        }
+        // MMA j: SFA in columns sf + 4j + c, SFB in columns sf + 16 + 8j + c
+        tmem_st4(sf + 0, a[0].x, a[1].x, a[2].x, a[3].x);
+        tmem_st4(sf + 4, a[0].y, a[1].y, a[2].y, a[3].y);
+        tmem_st4(sf + 8, a[0].z, a[1].z, a[2].z, a[3].z);
+        tmem_st4(sf + 12, a[0].w, a[1].w, a[2].w, a[3].w);
+        tmem_st4(sf + 16, b[0].x, b[1].x, b[2].x, b[3].x);
+        tmem_st4(sf + 20, b[4].x, b[5].x, b[6].x, b[7].x);
+        tmem_st4(sf + 24, b[0].y, b[1].y, b[2].y, b[3].y);
+        tmem_st4(sf + 28, b[4].y, b[5].y, b[6].y, b[7].y);
+        tmem_st4(sf + 32, b[0].z, b[1].z, b[2].z, b[3].z);
+        tmem_st4(sf + 36, b[4].z, b[5].z, b[6].z, b[7].z);
+        tmem_st4(sf + 40, b[0].w, b[1].w, b[2].w, b[3].w);
+        tmem_st4(sf + 44, b[4].w, b[5].w, b[6].w, b[7].w);
+    } else {
+        uint32_t a[4], b[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint32_t*>(ua + (lane + 32 * c) * 16 + 4 * sub);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) b[c] = *reinterpret_cast<const uint32_t*>(ub + (lane + 32 * c) * 16 + 4 * sub);
+        tmem_st4(sf + 0, a[0], a[1], a[2], a[3]);
+        tmem_st4(sf + 4, b[0], b[1], b[2], b[3]);
+        tmem_st4(sf + 8, b[4], b[5], b[6], b[7]);
+    }
+}
+
 template <int kKind>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm_pair_kernel(const __grid_constant__ Params p) {
-    constexpr int S = Pair<kKind>::kStages;
-    constexpr uint32_t kStage = pair_stage_bytes<kKind>();
+    constexpr int S = Pair<kKind>::S, G = Pair<kKind>::G, R = Pair<kKind>::R, DU = Pair<kKind>::DU,
+                  T = Pair<kKind>::T;
+    constexpr uint32_t kSfCols = Cfg<kKind>::kSfColsPerStage;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kStage);   // leader: pair TMA bytes
-    uint64_t* sf_full = full + S;                                        // own: scale staging
-    uint64_t* sf_ready = sf_full + S;                                    // leader: 8 writer warps
-    uint64_t* empty = sf_ready + S;                                      // own: multicast commit
-    uint64_t* accum = empty + S;                                         // own: multicast commit
+    uint8_t* sf_stage = smem + S * kPairStage;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sf_stage + R * kSfUnit);  // leader: pair TMA bytes
+    uint64_t* empty = full + S;                                              // own: multicast commit
+    uint64_t* sf_full = empty + S;                                           // own: scale TMA bytes
+    uint64_t* sf_empty = sf_full + R;                                      // own: 4 writer warps
+    uint64_t* sf_ready = sf_empty + R;                                     // leader: 8 writer warps
+    uint64_t* sf_free = sf_ready + T;                                      // own: multicast commit
+    uint64_t* accum = sf_free + T;                                         // own: multicast commit
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -626,9 +683,15 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);        // the leader's arrive.expect_tx (+ both CTAs' bytes)
-            mbar_init(&sf_full[i], 32);    // 32 producer-lane cp.async arrivals
-            mbar_init(&sf_ready[i], 8);    // 4 writer warps x 2 CTAs
             mbar_init(&empty[i], 1);       // the leader's multicast commit
+        }
+        for (int i = 0; i < R; ++i) {
+            mbar_init(&sf_full[i], 1);     // the producer's arrive.expect_tx
+            mbar_init(&sf_empty[i], 4);    // 4 writer warps have read the unit
+        }
+        for (int i = 0; i < T; ++i) {
+            mbar_init(&sf_ready[i], 8);    // 4 writer warps x 2 CTAs
+            mbar_init(&sf_free[i], 1);     // the leader's multicast commit
         }
         mbar_init(accum, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -651,36 +714,46 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tma_b) : "memory");
         }
         const uint64_t pol_a = l2_policy(p.m_fastest != 0), pol_b = l2_policy(p.m_fastest == 0);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int num_units = (p.num_kb + G - 1) / G;
+        const int sfb_row0 = p.b_sc_2d ? (int)(n0 >> 4) : (int)n0;
+        // scale unit u into staging slot u % R, once the writers have read its last use
+        auto load_sf = [&](int u) -> bool {
+            const int r = u % R;
+            if (!mbar_wait(&sf_empty[r], ((uint32_t)(u / R) & 1u) ^ 1u)) return false;
+            if (lane == 0) {
+                uint8_t* dst = sf_stage + r * kSfUnit;
+                mbar_arrive_expect_tx(&sf_full[r], kSfUnitA + (p.b_sc_2d ? 16u * 16u : kSfUnitB));
+                tma_load_2d(&p.tma_sfa, &sf_full[r], dst, u * 16, (int32_t)m0);
+                tma_load_2d(&p.tma_sfb, &sf_full[r], dst + kSfUnitA, u * 16, sfb_row0);
+            }
+            return true;
+        };
+        bool ok = true;
+        for (int u = 0; u < DU && u < num_units && ok; ++u) ok = load_sf(u);
+        for (int kb = 0; kb < p.num_kb && ok; ++kb) {
+            if (kb % G == 0 && kb / G + DU < num_units && !load_sf(kb / G + DU)) break;
             const int s = kb % S;
             if (!mbar_wait_pair(&empty[s], ((uint32_t)(kb / S) & 1u) ^ 1u)) break;
-            uint8_t* st = smem + s * kStage;
+            uint8_t* st = smem + s * kPairStage;
             if (lane == 0) {
-                if (leader) mbar_arrive_expect_tx(&full[s], 2 * (kABytes + kHalfBBytes));
+                if (leader) mbar_arrive_expect_tx(&full[s], 2 * kPairStage);
                 const uint32_t bar = leader_addr(&full[s]);
-                if (FP4Q_GEMM_L2_HINTS) {
-                    tma_load_2d_pair_hint(&p.tma_a, bar, st, kb * kBKBytes, (int32_t)m0, pol_a);
-                    tma_load_2d_pair_hint(&p.tma_b, bar, st + kABytes, kb * kBKBytes, (int32_t)(n0 + 128 * rank), pol_b);
-                } else {
-                    tma_load_2d_pair(&p.tma_a, bar, st, kb * kBKBytes, (int32_t)m0);
-                    tma_load_2d_pair(&p.tma_b, bar, st + kABytes, kb * kBKBytes, (int32_t)(n0 + 128 * rank));
-                }
+                tma_load_2d_pair_hint(&p.tma_a, bar, st, kb * kBKBytes, (int32_t)m0, pol_a);
+                tma_load_2d_pair_hint(&p.tma_b, bar, st + kABytes, kb * kBKBytes, (int32_t)(n0 + 128 * rank), pol_b);
             }
-            stage_scales<kKind>(p, p.b_sc, m0, n0, kb, smem_u32(st + kABytes + kHalfBBytes), lane);
-            cp_async_arrive_noinc(&sf_full[s]);
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer (leader only)
         if (leader && lane == 0) {
             for (int kb = 0; kb < p.num_kb; ++kb) {
-                const int s = kb % S;
-                const uint32_t ph = (uint32_t)(kb / S) & 1u;
-                if (!mbar_wait_pair(&full[s], ph) || !mbar_wait_pair(&sf_ready[s], ph)) break;
+                const int s = kb % S, t = kb % T;
+                if (!mbar_wait_pair(&full[s], (uint32_t)(kb / S) & 1u) ||
+                    !mbar_wait_pair(&sf_ready[t], (uint32_t)(kb / T) & 1u))
+                    break;
                 tc_fence_after();
-                const uint32_t sa = smem_u32(smem + s * kStage);
+                const uint32_t sa = smem_u32(smem + s * kPairStage);
                 const uint32_t sb = sa + kABytes;
-                const uint32_t sf_col = tmem + kSfCol + (uint32_t)s * Cfg<kKind>::kSfColsPerStage;
+                const uint32_t sf_col = tmem + kSfCol + (uint32_t)t * kSfCols;
                 if (kKind == 0) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
@@ -694,6 +767,7 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
                                    sf_col, sf_col + 4, (kb | j) ? 1u : 0u);
                 }
                 tc_commit_pair(&empty[s]);
+                if (T != S) tc_commit_pair(&sf_free[t]);   // T == S: the writers wait on `empty`
             }
             // both CTAs' accumulators are complete once every MMA above has finished
             tc_commit_pair(accum);
@@ -704,15 +778,19 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         const uint32_t ready0 = leader_addr(&sf_ready[0]);
         for (int kb = 0; kb < p.num_kb; ++kb) {
-            const int s = kb % S;
-            if (!mbar_wait(&sf_full[s], (uint32_t)(kb / S) & 1u)) break;
+            const int u = kb / G, r = u % R, t = kb % T;
+            if (!mbar_wait(&sf_full[r], (uint32_t)(u / R) & 1u)) break;
+            if (!mbar_wait_pair(T == S ? &empty[t] : &sf_free[t], ((uint32_t)(kb / T) & 1u) ^ 1u)) break;
             tc_fence_after();
-            const uint32_t sf = tmem + lane_base + kSfCol + (uint32_t)s * Cfg<kKind>::kSfColsPerStage;
-            write_stage_scales<kKind>(smem + s * kStage + kABytes + kHalfBBytes, sf, lane);
+            const uint32_t sf = tmem + lane_base + kSfCol + (uint32_t)t * kSfCols;
+            write_unit_scales<kKind>(sf_stage + r * kSfUnit, kb % G, p.b_sc_2d != 0, sf, lane);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(ready0 + (uint32_t)s * 8u);
+            if (lane == 0) {
+                mbar_arrive_cluster(ready0 + (uint32_t)t * 8u);
+                if (kb % G == G - 1 || kb == p.num_kb - 1) mbar_arrive(&sf_empty[r]);
+            }
         }
         const bool ok = mbar_wait_pair(accum, 0);
         tc_fence_after();
@@ -749,6 +827,19 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2D uint8 tensor map: [rows][row_bytes], box {128 B, box_rows}, 128-byte swizzle.
+// 2D uint8 tensor map over scale rows: [rows][row_bytes], box {16 B, box_rows}, no swizzle.
+bool make_map_sf(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {16, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -828,6 +919,11 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
     const uint64_t kbytes = kKind == 0 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
     if (!make_map(&p.tma_a, a.a, kbytes, (uint64_t)a.M, kBM)) return cudaErrorInvalidValue;
     if (!make_map(&p.tma_b, a.b, kbytes, (uint64_t)a.N, 128)) return cudaErrorInvalidValue;
+    const uint64_t sc_ld = kKind == 0 ? (uint64_t)a.K / 16 : (uint64_t)a.K / 32;
+    const bool b2d = kKind == 0 && a.b_scale_kind == 2;
+    if (!make_map_sf(&p.tma_sfa, a.a_scales, sc_ld, (uint64_t)a.M, kBM)) return cudaErrorInvalidValue;
+    if (!make_map_sf(&p.tma_sfb, a.b_scales, sc_ld, b2d ? (uint64_t)a.N / 16 : (uint64_t)a.N, b2d ? 16 : kBN))
+        return cudaErrorInvalidValue;
     p.a_sc = a.a_scales;
     p.b_sc = a.b_scales;
     p.sc_ld = kKind == 0 ? a.K / 16 : a.K / 32;
@@ -860,7 +956,11 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
 #endif
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     const int64_t stages = a.K / (a.kind == 0 ? Cfg<0>::kValuesPerStage : Cfg<1>::kValuesPerStage);
-    if (FP4Q_GEMM_PAIR && a.groups == 1 && a.M > 128 && stages >= 32)
+    // the pair kernel's scale TMA wants 16-byte aligned scale rows
+    const int64_t sc_ld = a.kind == 0 ? a.K / 16 : a.K / 32;
+    const bool sf_tma = sc_ld % 16 == 0 && ((reinterpret_cast<uintptr_t>(a.a_scales) |
+                                             reinterpret_cast<uintptr_t>(a.b_scales)) & 15u) == 0;
+    if (FP4Q_GEMM_PAIR && a.groups == 1 && a.M > 128 && stages >= 32 && sf_tma)
         return a.kind == 0 ? launch_pair<0>(a, st) : launch_pair<1>(a, st);
     return a.kind == 0 ? launch_kind<0>(a, st) : launch_kind<1>(a, st);
 }
