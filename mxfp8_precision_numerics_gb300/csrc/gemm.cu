@@ -371,6 +371,28 @@ __device__ __forceinline__ bool mbar_wait_pair(uint64_t* bar, uint32_t parity) {
         }
     }
 }
+// Bounded wait for warps that idle for a whole main loop (the epilogue): try_wait with a
+// suspend-time hint parks the warp until the phase completes instead of re-issuing.
+#ifndef FP4Q_IDLE_SUSPEND_NS
+#define FP4Q_IDLE_SUSPEND_NS 20000
+#endif
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p;}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"((uint32_t)FP4Q_IDLE_SUSPEND_NS) : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (FP4Q_IDLE_SUSPEND_NS > 0 ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait_pair(bar, parity))
+            return true;
+        if (globaltimer() - t0 > kTimeoutNs) {
+            atomicOr(&g_device_error, 1u);
+            return false;
+        }
+    }
+}
 // TMA load into this CTA's shared memory whose completion is counted on a barrier of the pair
 // (here always the leader's)
 __device__ __forceinline__ void tma_load_2d_pair_hint(const CUtensorMap* map, uint32_t bar_cluster_addr, void* dst,
@@ -558,44 +580,53 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
 
 // ------------------------------------------------------------------ the CTA-pair kernel
-// Two CTAs of a cluster compute one 256 x 256 output tile with tcgen05.mma.cta_group::2
-// (M = 256: each CTA owns 128 rows of A and of the accumulator; each holds 128 of the 256 B
-// rows, so each SM streams half the B tile of the single-CTA kernel: 32 KB instead of 48 KB
-// per stage for the same tensor-core work, and the ring holds 5-6 stages).
-//   producer (warp 4, each CTA): loads its A half and B half; completion is counted on the
-//     leader's `full` barrier (the leader posts the pair's transaction bytes); its lanes also
-//     cp.async this CTA's scale rows into staging (own `sf_full` barrier).
-//   scale writers (warps 0-3, each CTA): write this CTA's A rows and all 256 B rows of scales into
-//     its own tensor memory, then arrive on the leader's `sf_ready` barrier (8 arrivals).
-//   MMA issuer (warp 5 lane 0, leader only): 4 cta_group::2 MMAs per stage; the commit is
-//     multicast to both CTAs' `empty` barriers, and the final one to both `accum` barriers.
-//   epilogue (warps 0-3, each CTA): its own 128 accumulator rows.
+// Two CTAs of a cluster compute 256 x 256 output tiles with tcgen05.mma.cta_group::2 (M = 256:
+// each CTA owns 128 rows of A and of the accumulator and holds 128 of the 256 B rows, so each
+// SM streams 32 KB per stage instead of the single-CTA kernel's 48 KB for the same tensor-core
+// work). The kernel is persistent: cluster c takes tiles c, c + C, c + 2C, ...
+//   producer (warp 4, each CTA): A/B halves by TMA, completion counted on the leader's `full`
+//     barrier; this CTA's scale rows by TMA into a separate staging ring (own `sf_full`),
+//     running a few units ahead; both streams continue into the next tile without a break.
+//   scale writers (warps 0-3, each CTA): this CTA's A rows and all 256 B rows of scales into its
+//     own tensor memory, then an arrival on the leader's `sf_ready` barrier (8 arrivals).
+//   MMA issuer (warp 5 lane 0, leader only): waits for tensor memory to be free of the previous
+//     tile (`tmem_empty`), then 4 MMAs per K-block; commits are multicast to both CTAs.
+//   epilogue (warps 6-13, each CTA): copies its accumulator slice to registers, releases the
+//     tensor memory, then scales and stores while the next tile's MMAs run.
 // Pipeline depths of the pair kernel.
 //   S   A/B stages in shared memory (TMA, counted on the leader's `full` barrier)
-//   G   K-blocks per scale unit: one TMA box 16 bytes wide per operand holds the scales of
-//       G K-blocks for every row of the tile (4 x 4 E8M0 for MXFP8, 16 E4M3 for NVFP4)
+//   G   K-blocks per scale unit: one TMA box per operand holds the scales of G K-blocks for
+//       every row of the tile (W = G x the scale bytes of one K-block per row)
 //   R   scale units staged in shared memory
 //   DU  how many units the scale loads run ahead of the A/B loads
 //   T   scale slots in tensor memory (written by warps 0-3, read by the MMAs)
 // Scales travel by TMA (async proxy, no load/store-unit traffic: per-row 4-byte copies
-// through L1 took most of the shared-memory bandwidth the tensor core needs), their loads
-// run DU units ahead of the A/B loads and the writers may fill up to T tensor-memory slots
-// ahead of the MMAs. Tensor memory: 256 accumulator columns + T x kSfColsPerStage <= 512.
+// through L1 took most of the shared-memory bandwidth the tensor core needs) in boxes W bytes
+// wide: the TMA unit's cost grows with the rows of a box, so narrow scale boxes issued every
+// K-block held back the A/B loads. Their loads run DU units ahead of the A/B loads, and the
+// writers may fill up to T tensor-memory slots ahead of the MMAs.
+// Tensor memory: 256 accumulator columns + T x kSfColsPerStage <= 512.
 template <int kKind> struct Pair;
-template <> struct Pair<0> { static constexpr int S = 5, G = 1, R = 6, DU = 3, T = 5; };
+template <> struct Pair<0> { static constexpr int S = 5, G = 4, R = 2, DU = 1, T = 5; };
 template <> struct Pair<1> { static constexpr int S = 6, G = 4, R = 3, DU = 2, T = 16; };
 static_assert(256 + Pair<0>::T * Cfg<0>::kSfColsPerStage <= kTmemCols, "NVFP4 scale slots");
 static_assert(256 + Pair<1>::T * Cfg<1>::kSfColsPerStage <= kTmemCols, "MXFP8 scale slots");
 static_assert(Pair<0>::R >= Pair<0>::DU + 1 && Pair<1>::R >= Pair<1>::DU + 1, "scale ring depth");
 constexpr uint32_t kHalfBBytes = 128 * kBKBytes;   // 16 KB
 constexpr uint32_t kPairStage = kABytes + kHalfBBytes;   // 32 KB, 1024-aligned
-constexpr uint32_t kSfUnitA = kBM * 16;            // 2 KB: 128 A rows x 16 B
-constexpr uint32_t kSfUnitB = kBN * 16;            // 4 KB: 256 B rows x 16 B (2D tiles: 16 rows used)
-constexpr uint32_t kSfUnit = kSfUnitA + kSfUnitB;
+template <int kKind>
+__host__ __device__ constexpr uint32_t sf_unit_w() { return Pair<kKind>::G * Cfg<kKind>::kSfRowBytes; }
+template <int kKind>
+__host__ __device__ constexpr uint32_t sf_unit_a() { return kBM * sf_unit_w<kKind>(); }    // 128 A rows
+template <int kKind>
+__host__ __device__ constexpr uint32_t sf_unit_b() { return kBN * sf_unit_w<kKind>(); }    // 256 B rows
+template <int kKind>
+__host__ __device__ constexpr uint32_t sf_unit() { return sf_unit_a<kKind>() + sf_unit_b<kKind>(); }
+static_assert(sf_unit_w<0>() % 16 == 0 && sf_unit_w<1>() % 16 == 0, "scale box width");
 
 template <int kKind>
 __host__ __device__ constexpr uint32_t pair_smem_bytes() {
-    return Pair<kKind>::S * kPairStage + Pair<kKind>::R * kSfUnit + 1024 + 1024;
+    return Pair<kKind>::S * kPairStage + Pair<kKind>::R * sf_unit<kKind>() + 1024 + 1024;
 }
 static_assert(pair_smem_bytes<0>() <= 227 * 1024, "NVFP4 pair shared memory");
 static_assert(pair_smem_bytes<1>() <= 227 * 1024, "MXFP8 pair shared memory");
@@ -604,21 +635,22 @@ constexpr uint32_t kIdesc2Nvfp4 = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3)
 constexpr uint32_t kIdesc2Mxfp8 = (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                                   (1u << 23) | ((uint32_t)(256 >> 4) << 24);
 
-// Scale writer step of the pair kernel: K-block `sub` of a staged unit (rows 16 B apart) into
-// tensor memory, in the layout the tensor core reads (row r: lane r mod 32 of every lane
+// Scale writer step of the pair kernel: K-block `sub` of a staged unit (rows W bytes apart)
+// into tensor memory, in the layout the tensor core reads (row r: lane r mod 32 of every lane
 // quarter, column base + r/32). b2d: B holds one scale row per 16 rows (16 x 16 tiles).
 template <int kKind>
 __device__ __forceinline__ void write_unit_scales(const uint8_t* unit, int sub, bool b2d, uint32_t sf, int lane) {
-    const uint8_t* ua = unit;
-    const uint8_t* ub = unit + kSfUnitA;
+    constexpr uint32_t W = sf_unit_w<kKind>();
+    const uint8_t* ua = unit + sub * Cfg<kKind>::kSfRowBytes;
+    const uint8_t* ub = unit + sf_unit_a<kKind>() + sub * Cfg<kKind>::kSfRowBytes;
     if (kKind == 0) {
         uint4 a[4], b[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint4*>(ua + (lane + 32 * c) * 16);
+        for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint4*>(ua + (lane + 32 * c) * W);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             const int r = lane + 32 * c;
-            b[c] = *reinterpret_cast<const uint4*>(ub + (b2d ? (r >> 4) : r) * 16);
+            b[c] = *reinterpret_cast<const uint4*>(ub + (b2d ? (r >> 4) : r) * W);
         }
         // MMA j: SFA in columns sf + 4j + c, SFB in columns sf + 16 + 8j + c
         tmem_st4(sf + 0, a[0].x, a[1].x, a[2].x, a[3].x);
@@ -636,17 +668,96 @@ __device__ __forceinline__ void write_unit_scales(const uint8_t* unit, int sub, 
     } else {
         uint32_t a[4], b[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint32_t*>(ua + (lane + 32 * c) * 16 + 4 * sub);
+        for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint32_t*>(ua + (lane + 32 * c) * W);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) b[c] = *reinterpret_cast<const uint32_t*>(ub + (lane + 32 * c) * 16 + 4 * sub);
+        for (int c = 0; c < 8; ++c) b[c] = *reinterpret_cast<const uint32_t*>(ub + (lane + 32 * c) * W);
         tmem_st4(sf + 0, a[0], a[1], a[2], a[3]);
         tmem_st4(sf + 4, b[0], b[1], b[2], b[3]);
         tmem_st4(sf + 8, b[4], b[5], b[6], b[7]);
     }
 }
 
+// tcgen05.wait::ld that also names the destination registers, so that no use of them can be
+// scheduled before the wait
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+                   "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+                   "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :: "memory");
+}
+// tcgen05.ld of 32 columns without the wait
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32"
+                 " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+                   "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                   "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+                   "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr) : "memory");
+}
+
+// One row's 32 accumulator columns, scaled by alpha, stored as fp32 or bf16.
+__device__ __forceinline__ void store_chunk(const Params& p, const uint32_t (&r)[32], int64_t row, bool row_ok,
+                                            int64_t col, float alpha) {
+    if (!row_ok || col >= p.N) return;
+    const bool full32 = col + 32 <= p.N;
+    if (p.d_bf16) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha),
+                                                      __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
+            pk[i] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + row * p.N + col);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        if (full32) {
+            dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+            dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+        }
+    } else {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.N + col);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i >= 4 && !full32) break;
+            dst[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
+        }
+    }
+}
+
+// Output tile `tile` of the pair -> this CTA's first row and the tile's first column.
+__device__ __forceinline__ void pair_tile(const Params& p, int tile, uint32_t rank, int64_t& m0, int64_t& n0) {
+    int mt, nt;
+    if (p.m_fastest) {
+        nt = tile / p.m_tiles;
+        mt = tile - nt * p.m_tiles;
+    } else {
+        mt = tile / p.n_tiles;
+        nt = tile - mt * p.n_tiles;
+    }
+    m0 = (int64_t)mt * 256 + 128 * (int64_t)rank;
+    n0 = (int64_t)nt * kBN;
+}
+
+// Persistent CTA-pair GEMM: cluster c computes tiles c, c + C, c + 2C, ... (C clusters).
+// Warps: 0-3 scale writers, 4 producer, 5 MMA issuer (leader CTA), 6-13 epilogue (two per
+// tensor-memory lane quarter, 128 accumulator columns each). The epilogue copies the finished
+// accumulator to registers, releases it (tmem_empty) and stores while the next tile's MMAs run;
+// the producer and the writers run ahead into the next tile meanwhile.
+constexpr int kPairThreads = 448;
+
 template <int kKind>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 gemm_pair_kernel(const __grid_constant__ Params p) {
     constexpr int S = Pair<kKind>::S, G = Pair<kKind>::G, R = Pair<kKind>::R, DU = Pair<kKind>::DU,
                   T = Pair<kKind>::T;
@@ -654,31 +765,24 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sf_stage = smem + S * kPairStage;
+    constexpr uint32_t kSfUnit = sf_unit<kKind>(), kSfUnitA = sf_unit_a<kKind>(), kW = sf_unit_w<kKind>();
     uint64_t* full = reinterpret_cast<uint64_t*>(sf_stage + R * kSfUnit);  // leader: pair TMA bytes
     uint64_t* empty = full + S;                                              // own: multicast commit
     uint64_t* sf_full = empty + S;                                           // own: scale TMA bytes
-    uint64_t* sf_empty = sf_full + R;                                      // own: 4 writer warps
-    uint64_t* sf_ready = sf_empty + R;                                     // leader: 8 writer warps
-    uint64_t* sf_free = sf_ready + T;                                      // own: multicast commit
-    uint64_t* accum = sf_free + T;                                         // own: multicast commit
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+    uint64_t* sf_empty = sf_full + R;                                        // own: 4 writer warps
+    uint64_t* sf_ready = sf_empty + R;                                       // leader: 8 writer warps
+    uint64_t* sf_free = sf_ready + T;                                        // own: multicast commit
+    uint64_t* accum_full = sf_free + T;                                      // own: multicast commit
+    uint64_t* tmem_empty = accum_full + 1;                                   // leader: 16 epilogue warps
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
-
-    // ---- tile decode: cluster -> (256-row block, n tile); this CTA's rows m0 .. m0 + 127
-    const int c = blockIdx.x >> 1;
-    int mt, nt;
-    if (p.m_fastest) {
-        nt = c / p.m_tiles;
-        mt = c - nt * p.m_tiles;
-    } else {
-        mt = c / p.n_tiles;
-        nt = c - mt * p.n_tiles;
-    }
-    const int64_t m0 = (int64_t)mt * 256 + 128 * (int64_t)rank;
-    const int64_t n0 = (int64_t)nt * kBN;
+    const int cid = (int)(blockIdx.x >> 1), ncl = (int)(gridDim.x >> 1);
+    const int total_tiles = p.m_tiles * p.n_tiles;
+    const int my_tiles = cid < total_tiles ? (total_tiles - cid + ncl - 1) / ncl : 0;
+    const int total_kb = my_tiles * p.num_kb;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -693,7 +797,8 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
             mbar_init(&sf_ready[i], 8);    // 4 writer warps x 2 CTAs
             mbar_init(&sf_free[i], 1);     // the leader's multicast commit
         }
-        mbar_init(accum, 1);
+        mbar_init(accum_full, 1);          // the leader's multicast commit
+        mbar_init(tmem_empty, 16);         // 8 epilogue warps x 2 CTAs
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 5) {
@@ -712,28 +817,45 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tma_a) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tma_b) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tma_sfa) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&p.tma_sfb) : "memory");
         }
         const uint64_t pol_a = l2_policy(p.m_fastest != 0), pol_b = l2_policy(p.m_fastest == 0);
-        const int num_units = (p.num_kb + G - 1) / G;
-        const int sfb_row0 = p.b_sc_2d ? (int)(n0 >> 4) : (int)n0;
-        // scale unit u into staging slot u % R, once the writers have read its last use
-        auto load_sf = [&](int u) -> bool {
-            const int r = u % R;
-            if (!mbar_wait(&sf_empty[r], ((uint32_t)(u / R) & 1u) ^ 1u)) return false;
+        const int units_per_tile = p.num_kb / G;
+        const int total_units = my_tiles * units_per_tile;
+        // The scale stream runs ahead of the A/B stream; both track their tile incrementally
+        // (a runtime division per K-block on this lane would hold back the TMA issue).
+        int sf_u = 0, sf_uk = 0, sf_ti = 0;
+        int64_t sf_m0 = 0, sf_n0 = 0;
+        if (total_units > 0) pair_tile(p, cid, rank, sf_m0, sf_n0);
+        // next scale unit into staging slot sf_u % R, once the writers have read that slot's
+        // previous unit
+        auto load_next_sf = [&]() -> bool {
+            const int r = sf_u % R;
+            if (!mbar_wait(&sf_empty[r], ((uint32_t)(sf_u / R) & 1u) ^ 1u)) return false;
             if (lane == 0) {
                 uint8_t* dst = sf_stage + r * kSfUnit;
-                mbar_arrive_expect_tx(&sf_full[r], kSfUnitA + (p.b_sc_2d ? 16u * 16u : kSfUnitB));
-                tma_load_2d(&p.tma_sfa, &sf_full[r], dst, u * 16, (int32_t)m0);
-                tma_load_2d(&p.tma_sfb, &sf_full[r], dst + kSfUnitA, u * 16, sfb_row0);
+                mbar_arrive_expect_tx(&sf_full[r], kSfUnitA + (p.b_sc_2d ? 16u : (uint32_t)kBN) * kW);
+                tma_load_2d(&p.tma_sfa, &sf_full[r], dst, sf_uk * (int)kW, (int32_t)sf_m0);
+                tma_load_2d(&p.tma_sfb, &sf_full[r], dst + kSfUnitA, sf_uk * (int)kW,
+                            (int32_t)(p.b_sc_2d ? (sf_n0 >> 4) : sf_n0));
+            }
+            ++sf_u;
+            if (++sf_uk == units_per_tile) {
+                sf_uk = 0;
+                if (++sf_ti < my_tiles) pair_tile(p, cid + sf_ti * ncl, rank, sf_m0, sf_n0);
             }
             return true;
         };
         bool ok = true;
-        for (int u = 0; u < DU && u < num_units && ok; ++u) ok = load_sf(u);
-        for (int kb = 0; kb < p.num_kb && ok; ++kb) {
-            if (kb % G == 0 && kb / G + DU < num_units && !load_sf(kb / G + DU)) break;
-            const int s = kb % S;
-            if (!mbar_wait_pair(&empty[s], ((uint32_t)(kb / S) & 1u) ^ 1u)) break;
+        int issued = 0;
+        int64_t m0 = 0, n0 = 0;
+        for (int gk = 0, kb = 0, ti = 0; gk < total_kb && ok; ++gk) {
+            if (kb == 0) pair_tile(p, cid + ti * ncl, rank, m0, n0);
+            while (ok && sf_u < total_units && sf_u <= gk / G + DU) ok = load_next_sf();
+            if (!ok) break;
+            const int s = gk % S;
+            if (!mbar_wait_pair(&empty[s], ((uint32_t)(gk / S) & 1u) ^ 1u)) break;
             uint8_t* st = smem + s * kPairStage;
             if (lane == 0) {
                 if (leader) mbar_arrive_expect_tx(&full[s], 2 * kPairStage);
@@ -741,62 +863,132 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
                 tma_load_2d_pair_hint(&p.tma_a, bar, st, kb * kBKBytes, (int32_t)m0, pol_a);
                 tma_load_2d_pair_hint(&p.tma_b, bar, st + kABytes, kb * kBKBytes, (int32_t)(n0 + 128 * rank), pol_b);
             }
+            issued = gk + 1;
+            if (++kb == p.num_kb) {
+                kb = 0;
+                ++ti;
+            }
         }
+        // Every copy this CTA issued has landed before it may exit (on an early exit the
+        // consumers no longer wait for them). The leader's `full` counts both CTAs' A/B
+        // bytes; the follower is held at the final cluster barrier until the leader is done.
+        if (leader)
+            for (int gk = issued > S ? issued - S : 0; gk < issued; ++gk)
+                mbar_wait_pair(&full[gk % S], (uint32_t)(gk / S) & 1u);
+        for (int u = sf_u > R ? sf_u - R : 0; u < sf_u; ++u) mbar_wait(&sf_full[u % R], (uint32_t)(u / R) & 1u);
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer (leader only)
         if (leader && lane == 0) {
-            for (int kb = 0; kb < p.num_kb; ++kb) {
-                const int s = kb % S, t = kb % T;
-                if (!mbar_wait_pair(&full[s], (uint32_t)(kb / S) & 1u) ||
-                    !mbar_wait_pair(&sf_ready[t], (uint32_t)(kb / T) & 1u))
-                    break;
+            bool ok = true;
+            for (int ti = 0; ti < my_tiles && ok; ++ti) {
+                // the epilogue has copied the previous tile's accumulator out of tensor memory
+                if (!mbar_wait_pair(tmem_empty, ((uint32_t)ti & 1u) ^ 1u)) break;
                 tc_fence_after();
-                const uint32_t sa = smem_u32(smem + s * kPairStage);
-                const uint32_t sb = sa + kABytes;
-                const uint32_t sf_col = tmem + kSfCol + (uint32_t)t * kSfCols;
-                if (kKind == 0) {
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    const int gk = ti * p.num_kb + kb;
+                    const int s = gk % S, t = gk % T;
+                    if (!mbar_wait_pair(&full[s], (uint32_t)(gk / S) & 1u) ||
+                        !mbar_wait_pair(&sf_ready[t], (uint32_t)(gk / T) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + s * kPairStage);
+                    const uint32_t sb = sa + kABytes;
+                    const uint32_t sf_col = tmem + kSfCol + (uint32_t)t * kSfCols;
+                    if (kKind == 0) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        mma2_nvfp4(tmem + kAccCol, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
-                                   kIdesc2Nvfp4, sf_col + 4 * j, sf_col + 16 + 8 * j, (kb | j) ? 1u : 0u);
-                } else {
+                        for (int j = 0; j < 4; ++j)
+                            mma2_nvfp4(tmem + kAccCol, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
+                                       kIdesc2Nvfp4, sf_col + 4 * j, sf_col + 16 + 8 * j, (kb | j) ? 1u : 0u);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        mma2_mxfp8(tmem + kAccCol, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
-                                   kIdesc2Mxfp8 | ((uint32_t)j << 29) | ((uint32_t)j << 4),
-                                   sf_col, sf_col + 4, (kb | j) ? 1u : 0u);
+                        for (int j = 0; j < 4; ++j)
+                            mma2_mxfp8(tmem + kAccCol, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
+                                       kIdesc2Mxfp8 | ((uint32_t)j << 29) | ((uint32_t)j << 4),
+                                       sf_col, sf_col + 4, (kb | j) ? 1u : 0u);
+                    }
+                    tc_commit_pair(&empty[s]);
+                    if (T != S) tc_commit_pair(&sf_free[t]);   // T == S: the writers wait on `empty`
                 }
-                tc_commit_pair(&empty[s]);
-                if (T != S) tc_commit_pair(&sf_free[t]);   // T == S: the writers wait on `empty`
+                if (!ok) break;
+                // both CTAs' accumulators are complete once every MMA above has finished
+                tc_commit_pair(accum_full);
             }
-            // both CTAs' accumulators are complete once every MMA above has finished
-            tc_commit_pair(accum);
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------ warps 0-3: scale writers, then epilogue
+    } else if (warp < 4) {
+        // ------------------------------------------------ warps 0-3: scale writers
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         const uint32_t ready0 = leader_addr(&sf_ready[0]);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-            const int u = kb / G, r = u % R, t = kb % T;
+        for (int gk = 0; gk < total_kb; ++gk) {
+            const int u = gk / G, r = u % R, t = gk % T;
             if (!mbar_wait(&sf_full[r], (uint32_t)(u / R) & 1u)) break;
-            if (!mbar_wait_pair(T == S ? &empty[t] : &sf_free[t], ((uint32_t)(kb / T) & 1u) ^ 1u)) break;
+            if (!mbar_wait_pair(T == S ? &empty[t] : &sf_free[t], ((uint32_t)(gk / T) & 1u) ^ 1u)) break;
             tc_fence_after();
             const uint32_t sf = tmem + lane_base + kSfCol + (uint32_t)t * kSfCols;
-            write_unit_scales<kKind>(sf_stage + r * kSfUnit, kb % G, p.b_sc_2d != 0, sf, lane);
+            write_unit_scales<kKind>(sf_stage + r * kSfUnit, gk % G, p.b_sc_2d != 0, sf, lane);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive_cluster(ready0 + (uint32_t)t * 8u);
-                if (kb % G == G - 1 || kb == p.num_kb - 1) mbar_arrive(&sf_empty[r]);
+                if (gk % G == G - 1) mbar_arrive(&sf_empty[r]);
             }
         }
-        const bool ok = mbar_wait_pair(accum, 0);
-        tc_fence_after();
-        if (ok) {
-            const float alpha = kKind == 0 ? __fmul_rn(p.a_s_dec[0], p.b_s_dec[0]) : 1.0f;
-            store_tile(p, tmem + kAccCol, warp, lane, m0, p.M, n0, alpha);
+    } else {
+        // ------------------------------------------------ warps 6-13: epilogue
+        const int q = warp & 3, h = (warp - 6) >> 2;          // lane quarter, column half
+        const uint32_t tacc = tmem + kAccCol + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
+        const uint32_t empty_leader = leader_addr(tmem_empty);
+        const float alpha = kKind == 0 ? __fmul_rn(p.a_s_dec[0], p.b_s_dec[0]) : 1.0f;
+        for (int ti = 0; ti < my_tiles; ++ti) {
+            int64_t m0, n0;
+            pair_tile(p, cid + ti * ncl, rank, m0, n0);
+            if (!mbar_wait_idle(accum_full, (uint32_t)ti & 1u)) break;
+            tc_fence_after();
+            const int64_t row = m0 + 32 * q + lane;
+            const bool row_ok = row < p.M;
+            const int64_t col0 = n0 + 128 * h;
+            if (kKind == 1) {
+                // MXFP8: the slice's 128 columns into registers with one wait, tensor memory back
+                // to the MMAs, then scale and store
+                uint32_t r0[32], r1[32], r2[32], r3[32];
+                tmem_ld32_async(tacc, r0);
+                tmem_ld32_async(tacc + 32, r1);
+                tmem_ld32_async(tacc + 64, r2);
+                tmem_ld32_async(tacc + 96, r3);
+                tmem_wait_ld(r0);
+                tmem_wait_ld(r1);
+                tmem_wait_ld(r2);
+                tmem_wait_ld(r3);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(empty_leader);
+                store_chunk(p, r0, row, row_ok, col0, alpha);
+                store_chunk(p, r1, row, row_ok, col0 + 32, alpha);
+                store_chunk(p, r2, row, row_ok, col0 + 64, alpha);
+                store_chunk(p, r3, row, row_ok, col0 + 96, alpha);
+            } else {
+                // NVFP4: loads interleaved with the stores of the previous chunk, so that most of
+                // the output traffic is out before the next tile's operand stream restarts
+                uint32_t ra[32], rb[32];
+                tmem_ld32_async(tacc, ra);
+                tmem_wait_ld(ra);
+                tmem_ld32_async(tacc + 32, rb);
+                store_chunk(p, ra, row, row_ok, col0, alpha);
+                tmem_wait_ld(rb);
+                tmem_ld32_async(tacc + 64, ra);
+                store_chunk(p, rb, row, row_ok, col0 + 32, alpha);
+                tmem_wait_ld(ra);
+                tmem_ld32_async(tacc + 96, rb);
+                store_chunk(p, ra, row, row_ok, col0 + 64, alpha);
+                tmem_wait_ld(rb);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(empty_leader);
+                store_chunk(p, rb, row, row_ok, col0 + 96, alpha);
+            }
         }
     }
 
@@ -827,13 +1019,14 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2D uint8 tensor map: [rows][row_bytes], box {128 B, box_rows}, 128-byte swizzle.
-// 2D uint8 tensor map over scale rows: [rows][row_bytes], box {16 B, box_rows}, no swizzle.
-bool make_map_sf(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+// 2D uint8 tensor map over scale rows: [rows][row_bytes], box {box_w B, box_rows}, no swizzle.
+bool make_map_sf(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_w,
+                 uint32_t box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {row_bytes, rows};
     cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {16, box_rows};
+    cuuint32_t box[2] = {box_w, box_rows};
     cuuint32_t es[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -921,8 +1114,10 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
     if (!make_map(&p.tma_b, a.b, kbytes, (uint64_t)a.N, 128)) return cudaErrorInvalidValue;
     const uint64_t sc_ld = kKind == 0 ? (uint64_t)a.K / 16 : (uint64_t)a.K / 32;
     const bool b2d = kKind == 0 && a.b_scale_kind == 2;
-    if (!make_map_sf(&p.tma_sfa, a.a_scales, sc_ld, (uint64_t)a.M, kBM)) return cudaErrorInvalidValue;
-    if (!make_map_sf(&p.tma_sfb, a.b_scales, sc_ld, b2d ? (uint64_t)a.N / 16 : (uint64_t)a.N, b2d ? 16 : kBN))
+    if (!make_map_sf(&p.tma_sfa, a.a_scales, sc_ld, (uint64_t)a.M, sf_unit_w<kKind>(), kBM))
+        return cudaErrorInvalidValue;
+    if (!make_map_sf(&p.tma_sfb, a.b_scales, sc_ld, b2d ? (uint64_t)a.N / 16 : (uint64_t)a.N, sf_unit_w<kKind>(),
+                     b2d ? 16 : kBN))
         return cudaErrorInvalidValue;
     p.a_sc = a.a_scales;
     p.b_sc = a.b_scales;
@@ -941,8 +1136,23 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
     p.groups = 1;
     const double a_bytes = (double)a.M * (double)kbytes, b_bytes = (double)a.N * (double)kbytes;
     p.m_fastest = a_bytes < b_bytes ? 1 : 0;
-    const int64_t clusters = (int64_t)p.m_tiles * p.n_tiles;
-    gemm_pair_kernel<kKind><<<(unsigned)(2 * clusters), kThreads, pair_smem_bytes<kKind>(), st>>>(p);
+    const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
+    static int max_clusters[2] = {0, 0};
+    if (max_clusters[kKind] <= 0) {
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(2 * (unsigned)(num_sms() / 2), 1, 1);
+        cfg.blockDim = dim3(kPairThreads, 1, 1);
+        cfg.dynamicSmemBytes = pair_smem_bytes<kKind>();
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<kKind>, &cfg) != cudaSuccess || n < 1) {
+            (void)cudaGetLastError();
+            n = num_sms() / 2;
+        }
+        max_clusters[kKind] = n;
+    }
+    const int64_t clusters = tiles < max_clusters[kKind] ? tiles : max_clusters[kKind];
+    gemm_pair_kernel<kKind><<<(unsigned)(2 * clusters), kPairThreads, pair_smem_bytes<kKind>(), st>>>(p);
     return cudaGetLastError();
 }
 
@@ -954,13 +1164,18 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
 #ifndef FP4Q_GEMM_PAIR
 #define FP4Q_GEMM_PAIR 1
 #endif
+#ifndef FP4Q_PAIR_MIN_STAGES
+#define FP4Q_PAIR_MIN_STAGES 1
+#endif
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     const int64_t stages = a.K / (a.kind == 0 ? Cfg<0>::kValuesPerStage : Cfg<1>::kValuesPerStage);
     // the pair kernel's scale TMA wants 16-byte aligned scale rows
     const int64_t sc_ld = a.kind == 0 ? a.K / 16 : a.K / 32;
-    const bool sf_tma = sc_ld % 16 == 0 && ((reinterpret_cast<uintptr_t>(a.a_scales) |
-                                             reinterpret_cast<uintptr_t>(a.b_scales)) & 15u) == 0;
-    if (FP4Q_GEMM_PAIR && a.groups == 1 && a.M > 128 && stages >= 32 && sf_tma)
+    // and whole scale units per tile
+    const int64_t g_units = a.kind == 0 ? Pair<0>::G : Pair<1>::G;
+    const bool sf_tma = sc_ld % 16 == 0 && stages % g_units == 0 &&
+                        ((reinterpret_cast<uintptr_t>(a.a_scales) | reinterpret_cast<uintptr_t>(a.b_scales)) & 15u) == 0;
+    if (FP4Q_GEMM_PAIR && a.groups == 1 && a.M > 128 && stages >= FP4Q_PAIR_MIN_STAGES && sf_tma)
         return a.kind == 0 ? launch_pair<0>(a, st) : launch_pair<1>(a, st);
     return a.kind == 0 ? launch_kind<0>(a, st) : launch_kind<1>(a, st);
 }
