@@ -272,30 +272,64 @@ def run_ours(args, rank, world, local_rank):
     kinds = log.totals()
 
     # ---- end to end through the public API with host buffers (pinned)
-    # every step copies its inputs in from pinned host memory and its results (Y, dX, dW1,
-    # dW2) back out; the device-side events and the host wall clock bracket the loop
+    # Every step copies its inputs in from pinned host memory and its results (Y, dX, dW1, dW2)
+    # back out, as a training loop feeding the layer from the host would: a copy stream brings
+    # step i+1's inputs in while step i computes and takes step i's results out as they are
+    # done. Device buffers and pinned result buffers are allocated before the timed loop. The
+    # device events and the host wall clock bracket the loop.
+    e2e_steps = max(1, args.steps // 2)
+    copy = torch.cuda.Stream(device=dev)
+    comp = torch.cuda.current_stream(dev)
+    dbuf = [[torch.empty_like(t, device=dev) for t in host] for _ in range(2)]
     outs_host = None
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = 0
+
+    def e2e_loop(nsteps):
+        nonlocal outs_host, d2h
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        buf_free = [torch.cuda.Event() for _ in range(2)]
+        out_done = torch.cuda.Event()
+        with torch.cuda.stream(copy):
+            for d, hsrc in zip(dbuf[0], host):
+                d.copy_(hsrc, non_blocking=True)
+            in_ready[0].record(copy)
+        for i in range(nsteps):
+            b = i % 2
+            comp.wait_event(in_ready[b])
+            outs = mlp_step(F, torch, dbuf[b], log, seed, signs)
+            buf_free[b].record(comp)
+            out_done.record(comp)
+            with torch.cuda.stream(copy):
+                if i + 1 < nsteps:
+                    nb = (i + 1) % 2
+                    if i >= 1:
+                        copy.wait_event(buf_free[nb])
+                    for d, hsrc in zip(dbuf[nb], host):
+                        d.copy_(hsrc, non_blocking=True)
+                    in_ready[nb].record(copy)
+                copy.wait_event(out_done)
+                if outs_host is None:
+                    outs_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+                for oh, o in zip(outs_host, outs):
+                    o.record_stream(copy)
+                    oh.copy_(o, non_blocking=True)
+            d2h = sum(o.numel() * o.element_size() for o in outs)
+        comp.wait_stream(copy)
+
+    e2e_loop(2)                      # warm-up: allocations and first-touch outside the timing
+    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    e0.record()
-    h2d = d2h = 0
-    for _ in range(max(1, args.steps // 2)):
-        dins = [t.to(dev, non_blocking=True) for t in host]
-        h2d = sum(t.numel() * t.element_size() for t in host)
-        outs = mlp_step(F, torch, dins, log, seed, signs)
-        if outs_host is None:
-            outs_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-        for oh, o in zip(outs_host, outs):
-            oh.copy_(o, non_blocking=True)
-        d2h = sum(o.numel() * o.element_size() for o in outs)
-    e1.record()
+    e0.record(comp)
+    e2e_loop(e2e_steps)
+    e1.record(comp)
     torch.cuda.synchronize()
     wall1 = time.perf_counter()
     barrier()
-    e2e_steps = max(1, args.steps // 2)
     e2e_ms = max(e0.elapsed_time(e1), (wall1 - wall0) * 1e3) / e2e_steps
     st = F.fp4q_device_status()
     if st != F.OK:

@@ -89,6 +89,10 @@ __device__ __forceinline__ int mx_exponent(float amax) {
     return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
+// 2^k as fp32 for k in [-149, 127] (k < -126: subnormal powers of two).
+__device__ __forceinline__ float exp2i_wide(int k) {
+    return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(1u << (k + 149));
+}
 // 2^k as fp32 for k in [-127, 127] (2^-127 is the subnormal 0x00400000).
 __device__ __forceinline__ float exp2i(int k) {
     return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(0x00400000u);
@@ -203,8 +207,8 @@ __device__ __forceinline__ uint32_t bf16_sign_mask2(uint32_t signs, int p) {
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-        uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
         c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
@@ -228,7 +232,20 @@ __device__ __forceinline__ uint32_t slice16(uint4 w, int j) {
 // distances 1, 2, 4, 8 (Sylvester H16 = H2 (x) H8), then the exact scaling by 1/4.
 // ("Pretraining Large Language Models with NVFP4", "Random Hadamard Transforms".)
 // ---------------------------------------------------------------------------------------
-// fwht16_quarter is the same without the sign step, for inputs already sign-flipped.
+// fwht16 is the butterflies alone (no signs, no 1/4); fwht16_quarter adds the 1/4.
+__device__ __forceinline__ void fwht16(float* v) {
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if ((i & h) == 0) {
+                float a = v[i], b = v[i + h];
+                v[i] = __fadd_rn(a, b);
+                v[i + h] = __fsub_rn(a, b);
+            }
+        }
+    }
+}
 __device__ __forceinline__ void fwht16_quarter(float* v) {
 #pragma unroll
     for (int h = 1; h < 16; h <<= 1) {

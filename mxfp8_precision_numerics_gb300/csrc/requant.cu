@@ -23,20 +23,38 @@ namespace fp4q {
 
 // Quantize 32 fp32 values (one MXFP8 block) and store 32 E4M3 bytes + 1 E8M0 byte.
 // kRht: the block is two transform groups whose sign flips the caller has already applied;
-// the butterflies and the 1/4 scaling happen here.
+// the butterflies happen here. The transform's 1/4 is folded into the block's power-of-two
+// scale, t = s * 2^(-e-2), which is the definition's fl(fl(s/4) * 2^-e) bit for bit whenever
+// max|s| >= 2^-88: then every s with s/4 in the fp32 normal range gives the same single
+// rounding of s * 2^(-e-2), and every smaller s gives |t| < 2^-27 under both orders, which
+// rounds (to nearest or stochastically, U <= 1 - 2^-16) to a zero of the same sign.
+// Blocks below that take the definition's order literally.
 template <bool kRht, bool kSR>
 __device__ __forceinline__ void mx_encode_block(float (&v)[32], uint64_t seed, uint32_t tag,
                                                 uint64_t out_idx0, uint8_t* __restrict__ out32,
                                                 uint8_t* __restrict__ out_sc) {
     if (kRht) {
-        fwht16_quarter(v);
-        fwht16_quarter(v + 16);
+        fwht16(v);
+        fwht16(v + 16);
     }
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    const int e = mx_exponent(amax);
-    const float inv = exp2i(-e);
+    int e;
+    float inv;
+    if (kRht) {
+        e = mx_exponent(__fmul_rn(amax, 0.25f));        // max|s/4| = max|s| / 4 (monotone rounding)
+        if (__float_as_uint(amax) >= 0x13800000u) {     // max|s| >= 2^-88
+            inv = exp2i_wide(-e - 2);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+            inv = exp2i(-e);
+        }
+    } else {
+        e = mx_exponent(amax);
+        inv = exp2i(-e);
+    }
     uint32_t words[8];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
@@ -117,73 +135,203 @@ __global__ void __launch_bounds__(256) requant_rows_kernel(RequantArgs a) {
     }
 }
 
-// ---------------------------------------------------------------------------------------
-// transpose = 1: 64 x 64 input tile per CTA, 128 threads. The transform groups run along
-// the input's rows (the output's contiguous dimension), so the sign of input row r is
-// that of position r mod 16 and is applied to whole packed words at load time.
-// ---------------------------------------------------------------------------------------
-constexpr int kTR = 64, kTC = 64, kPad = 1;
-
-template <int kKind, bool kRht, bool kSR>
-__global__ void __launch_bounds__(128) requant_t_kernel(RequantArgs a) {
-    __shared__ float tile[kTR][kTC + kPad];
-    const int64_t r0 = (int64_t)blockIdx.y * kTR;   // input rows   = output columns
-    const int64_t c0 = (int64_t)blockIdx.x * kTC;   // input columns = output rows
-    const int tid = threadIdx.x;
-
-    // ---- load + dequantize into shared memory (row-major, input orientation)
-    if (kKind == 0) {
-        const uint16_t* in = static_cast<const uint16_t*>(a.in);
+// Half of an MXFP8 block: this lane's 16 values (one transform group), the other 16 in the
+// partner lane (lane ^ 1); the block amax is combined with one shuffle. Same arithmetic as
+// mx_encode_block. Every lane of the warp must call it (stores are predicated on `valid`).
+// out_idx: output index of this lane's first value; out_sc: the block's E8M0 byte, written by
+// the lane holding the first half (nullptr in the other).
+template <bool kRht, bool kSR>
+__device__ __forceinline__ void mx_encode_half(float (&v)[16], bool valid, uint64_t seed, uint32_t tag,
+                                               uint64_t out_idx, uint8_t* __restrict__ out16,
+                                               uint8_t* __restrict__ out_sc) {
+    if (kRht) fwht16(v);
+    float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int v = tid + 128 * i;          // 512 vectors of 8 bf16
-            const int rr = v >> 3, cc = (v & 7) * 8;
-            float* dst = &tile[rr][cc];
-            if (r0 + rr < a.rows && c0 + cc < a.cols) {
-                const uint32_t m = kRht ? ((a.rht_signs >> (rr & 15)) & 1u) * 0x80008000u : 0u;
-                uint4 p = __ldcs(reinterpret_cast<const uint4*>(in + (r0 + rr) * a.cols + c0 + cc));
-                bf16x2_to_f32(p.x ^ m, dst);
-                bf16x2_to_f32(p.y ^ m, dst + 2);
-                bf16x2_to_f32(p.z ^ m, dst + 4);
-                bf16x2_to_f32(p.w ^ m, dst + 6);
-            }
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    int e;
+    float inv;
+    if (kRht) {
+        e = mx_exponent(__fmul_rn(amax, 0.25f));
+        if (__float_as_uint(amax) >= 0x13800000u) {     // max|s| >= 2^-88: fold the 1/4
+            inv = exp2i_wide(-e - 2);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+            inv = exp2i(-e);
         }
     } else {
-        const int rr = tid >> 1, half = tid & 1;
-        const int64_t gr = r0 + rr, gc = c0 + 32 * half;
-        if (gr < a.rows && gc < a.cols) {
-            const float s_dec = *a.in_s_dec;
-            const uint32_t m = kRht ? ((a.rht_signs >> (rr & 15)) & 1u) * 0x88888888u : 0u;
-            const uint4 c = __ldcs(reinterpret_cast<const uint4*>(
-                static_cast<const uint8_t*>(a.in) + gr * (a.cols >> 1) + (gc >> 1)));
-            uint32_t s0, s1;
-            if (kKind == 1) {
-                s0 = a.in_scales[gr * (a.cols >> 4) + (gc >> 4)];
-                s1 = a.in_scales[gr * (a.cols >> 4) + (gc >> 4) + 1];
-            } else {
-                s0 = a.in_scales[(gr >> 4) * (a.cols >> 4) + (gc >> 4)];
-                s1 = a.in_scales[(gr >> 4) * (a.cols >> 4) + (gc >> 4) + 1];
-            }
-            const uint32_t f0 = e4m3_to_f16x2_dup(s0), f1 = e4m3_to_f16x2_dup(s1);
-            float* dst = &tile[rr][32 * half];
-            dequant8_f16(c.x ^ m, f0, s_dec, dst);
-            dequant8_f16(c.y ^ m, f0, s_dec, dst + 8);
-            dequant8_f16(c.z ^ m, f1, s_dec, dst + 16);
-            dequant8_f16(c.w ^ m, f1, s_dec, dst + 24);
+        e = mx_exponent(amax);
+        inv = exp2i(-e);
+    }
+    uint32_t words[4];
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        float t[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) t[j] = __fmul_rn(v[8 * g + j], inv);
+        if (kSR) {
+            const uint4 r = sr_block8(seed, tag, (out_idx >> 3) + (uint64_t)g);
+            words[2 * g] = __byte_perm(e4m3x2_sr_hw(t[0], t[1], r.x), e4m3x2_sr_hw(t[2], t[3], r.y), 0x6420);
+            words[2 * g + 1] = __byte_perm(e4m3x2_sr_hw(t[4], t[5], r.z), e4m3x2_sr_hw(t[6], t[7], r.w), 0x6420);
+        } else {
+            words[2 * g] = e4m3x4_rn_hw(t[0], t[1], t[2], t[3]);
+            words[2 * g + 1] = e4m3x4_rn_hw(t[4], t[5], t[6], t[7]);
         }
     }
-    __syncthreads();
+    if (valid) {
+        __stcs(reinterpret_cast<uint4*>(out16), make_uint4(words[0], words[1], words[2], words[3]));
+        if (out_sc) *out_sc = (uint8_t)(e + 127);
+    }
+}
 
-    // ---- one output block per thread: output row c0 + c, output columns r0 + 32*blk + [0, 32)
-    const int c = tid & 63, blk = tid >> 6;
-    const int64_t orow = c0 + c, ocol = r0 + 32 * blk;
-    if (orow < a.cols && ocol < a.rows) {
-        float v[32];
+// ---------------------------------------------------------------------------------------
+// transpose = 1. Persistent CTAs of 256 threads walk 64 x 128 input tiles; each tile's raw
+// input (bf16 16 KB, or NVFP4 codes 4 KB) is brought into shared memory by cp.async one tile
+// ahead, its block scales by plain loads one tile ahead. Thread (p, g) owns input columns 2p
+// and 2p+1 of input rows 16g .. 16g+15: one transform group of one MXFP8 block of each of
+// two output rows; one 32-bit word (bf16 pair) or one byte (E2M1 pair) per input row feeds
+// both. Lanes 4p .. 4p+3 hold g = 0..3, so the two halves of a block sit in lanes l, l^1.
+// Shared memory is XOR-swizzled by row group (bf16: 8 words, codes: 16 bytes, scales: 2
+// entries) so that the four row groups reading one column pair hit distinct banks.
+// The transform groups run along the input's rows (the output's contiguous dimension), so
+// the sign of input row r is that of position r mod 16: for bf16 it is XORed onto the word,
+// for NVFP4 it is folded into that row's block scale (E2M1 x (-scale) is exact).
+// ---------------------------------------------------------------------------------------
+constexpr int kTR = 64, kTC = 128, kTThreads = 256;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kN>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(kN) : "memory"); }
+
+template <int kKind>
+struct TStage {
+    static constexpr uint32_t kBytes = kKind == 0 ? kTR * kTC * 2 : kTR * kTC / 2;   // 16 KB / 4 KB
+};
+
+template <int kKind, bool kRht, bool kSR>
+__global__ void __launch_bounds__(kTThreads) requant_t_kernel(RequantArgs a, int tiles_c, int n_tiles) {
+    __shared__ __align__(16) uint8_t stage[2][TStage<kKind>::kBytes];
+    __shared__ uint32_t sct[2][kKind == 0 ? 1 : kTR][8];   // per input row: f16x2 scales, signs folded
+    const int tid = threadIdx.x;
+    const int p = tid >> 2, grp = tid & 3, hb = grp & 1;
+    const float s_dec = (kKind == 0) ? 1.0f : *a.in_s_dec;
+    const int64_t sc_ld = a.cols >> 4;
+
+    // cp.async of tile `tile` into buffer `buf`; block scales of the tile into `sreg`
+    auto issue = [&](int tile, int buf, uint32_t (&sreg)[2]) {
+        const int tr = tile / tiles_c, tc = tile - tr * tiles_c;
+        const int64_t r0 = (int64_t)tr * kTR, c0 = (int64_t)tc * kTC;
+        const uint32_t base = (uint32_t)__cvta_generic_to_shared(&stage[buf][0]);
+        if (kKind == 0) {
+            const uint16_t* in = static_cast<const uint16_t*>(a.in);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = tile[32 * blk + k][c];
-        const int64_t oidx = orow * a.rows + ocol;
-        mx_encode_block<kRht, kSR>(v, a.seed, a.tag, (uint64_t)oidx,
-                                   a.out_e4m3 + oidx, a.out_e8m0 + (oidx >> 5));
+            for (int i = 0; i < 4; ++i) {
+                const int ch = tid + kTThreads * i;          // 1024 chunks of 8 bf16 (4 words)
+                const int row = ch >> 4, cw = (ch & 15) * 4;
+                const bool ok = r0 + row < a.rows && c0 + 2 * cw < a.cols;
+                const uint32_t dst = base + 4u * (uint32_t)(row * 64 + (cw ^ (8 * ((row >> 4) & 3))));
+                cp_async16(dst, in + (ok ? (r0 + row) * a.cols + c0 + 2 * cw : 0), ok);
+            }
+        } else {
+            const uint8_t* in = static_cast<const uint8_t*>(a.in);
+            const int row = tid >> 2, cb = (tid & 3) * 16;   // 256 chunks of 32 codes
+            const bool ok = r0 + row < a.rows && c0 + 2 * cb < a.cols;
+            const uint32_t dst = base + (uint32_t)(row * 64 + (cb ^ (16 * ((row >> 4) & 3))));
+            cp_async16(dst, in + (ok ? (r0 + row) * (a.cols >> 1) + (c0 >> 1) + cb : 0), ok);
+            // block scale of each input row and block of 16 columns (2D: the row's 16 x 16 tile)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int idx = tid + kTThreads * i;
+                const int srow = idx >> 3, blk = idx & 7;
+                const int64_t grow = r0 + srow, gcol = (c0 >> 4) + blk;
+                sreg[i] = 0;
+                if (grow < a.rows && gcol < sc_ld)
+                    sreg[i] = a.in_scales[(kKind == 2 ? (grow >> 4) : grow) * sc_ld + gcol];
+            }
+        }
+        cp_async_commit();
+    };
+
+    int tile = blockIdx.x;
+    if (tile >= n_tiles) return;
+    uint32_t sreg[2] = {0, 0};
+    issue(tile, 0, sreg);
+    for (int it = 0; tile < n_tiles; ++it, tile += gridDim.x) {
+        const int buf = it & 1;
+        if (kKind != 0) {
+            // this tile's scales -> f16x2 (both halves), with the sign of the row's transform
+            // position folded in
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int idx = tid + kTThreads * i;
+                const int srow = idx >> 3, blk = idx & 7;
+                uint32_t h = e4m3_to_f16x2_dup(sreg[i]);
+                if (kRht) h ^= ((a.rht_signs >> (srow & 15)) & 1u) * 0x80008000u;
+                sct[buf][srow][blk ^ (2 * ((srow >> 4) & 3))] = h;
+            }
+        }
+        const int next = tile + gridDim.x;
+        if (next < n_tiles) {
+            issue(next, buf ^ 1, sreg);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+
+        const int tr = tile / tiles_c, tc = tile - tr * tiles_c;
+        const int64_t r0 = (int64_t)tr * kTR, c0 = (int64_t)tc * kTC;
+        const int64_t orow = c0 + 2 * p, ocol = r0 + 32 * (grp >> 1);
+        const bool valid = orow < a.cols && ocol < a.rows;     // the same for both halves of a block
+        if (kKind == 0) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(&stage[buf][0]) + (16 * grp) * 64 + (p ^ (8 * grp));
+            uint32_t w[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                w[k] = src[k * 64];
+                if (kRht) w[k] ^= ((a.rht_signs >> k) & 1u) * 0x80008000u;
+            }
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                const uint32_t sh = half ? 0u : 16u;     // even column: low bf16, odd: high
+                float v[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) v[k] = __uint_as_float((w[k] << sh) & 0xFFFF0000u);
+                const int64_t oidx = (orow + half) * a.rows + ocol + 16 * hb;
+                mx_encode_half<kRht, kSR>(v, valid, a.seed, a.tag, (uint64_t)oidx, a.out_e4m3 + oidx,
+                                          hb ? nullptr : a.out_e8m0 + (oidx >> 5));
+            }
+        } else {
+            const uint8_t* src = &stage[buf][0] + (16 * grp) * 64 + (p ^ (16 * grp));
+            const uint32_t* sc = &sct[buf][16 * grp][(p >> 3) ^ (2 * grp)];
+            uint32_t h[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                h[k] = e2m1x2_to_f16x2(src[k * 64]);
+                asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[k]) : "r"(sc[k * 8]));
+            }
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                const uint32_t sel = half ? 0x3232u : 0x1010u;   // the column's f16 in both halves
+                float v[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    float f;
+                    asm("{.reg .f16 l, u; mov.b32 {l, u}, %1; cvt.f32.f16 %0, l;}"
+                        : "=f"(f) : "r"(__byte_perm(h[k], 0u, sel)));
+                    v[k] = __fmul_rn(f, s_dec);
+                }
+                const int64_t oidx = (orow + half) * a.rows + ocol + 16 * hb;
+                mx_encode_half<kRht, kSR>(v, valid, a.seed, a.tag, (uint64_t)oidx, a.out_e4m3 + oidx,
+                                          hb ? nullptr : a.out_e8m0 + (oidx >> 5));
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -229,8 +377,20 @@ __global__ void __launch_bounds__(256) rht16_kernel(const void* __restrict__ in,
 template <int kKind, bool kRht, bool kSR>
 static void launch_requant_t(const RequantArgs& a, cudaStream_t st) {
     if (a.transpose) {
-        dim3 grid((unsigned)((a.cols + kTC - 1) / kTC), (unsigned)((a.rows + kTR - 1) / kTR));
-        requant_t_kernel<kKind, kRht, kSR><<<grid, 128, 0, st>>>(a);
+        const int64_t tiles_c = (a.cols + kTC - 1) / kTC, tiles_r = (a.rows + kTR - 1) / kTR;
+        const int64_t n_tiles = tiles_c * tiles_r;
+        static int per_sm[3][2][2] = {};
+        int& occ = per_sm[kKind][kRht ? 1 : 0][kSR ? 1 : 0];
+        if (occ <= 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, requant_t_kernel<kKind, kRht, kSR>, kTThreads, 0) !=
+                    cudaSuccess || occ < 1) {
+                (void)cudaGetLastError();
+                occ = 4;
+            }
+        }
+        int64_t g = (int64_t)num_sms() * occ;
+        if (g > n_tiles) g = n_tiles;
+        requant_t_kernel<kKind, kRht, kSR><<<(unsigned)g, kTThreads, 0, st>>>(a, (int)tiles_c, (int)n_tiles);
     } else {
         int64_t items = a.rows * (a.cols / 32);
         int64_t g = (items + 255) / 256;
