@@ -58,14 +58,9 @@ def load_peaks():
         return dict(FALLBACK), "fallback"
 
 
-def source_sha(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
-
-
 def ncu_traffic(kind):
-    """DRAM bytes per launch of `kind` from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+    """DRAM bytes per launch of `kind` from the committed ncu summary, or None when any of
+    the kernel's sources changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -74,8 +69,14 @@ def ncu_traffic(kind):
         return None
     if not rec:
         return None
-    src = os.path.join(ROOT, "mxfp8_precision_numerics_gb300", "csrc", rec["source"])
-    if not os.path.exists(src) or source_sha(src) != rec["source_sha"]:
+    h = hashlib.sha256()
+    for name in rec["sources"]:
+        src = os.path.join(ROOT, "mxfp8_precision_numerics_gb300", "csrc", name)
+        if not os.path.exists(src):
+            return None
+        with open(src, "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != rec["source_sha"]:
         return None
     return rec["dram_bytes_per_launch"]
 
@@ -356,6 +357,8 @@ def run_ours(args, rank, world, local_rank):
             kernels[kind] = {"launches": n, "avg_ms": round(avg, 4), "achieved": round(gbs, 1),
                              "unit": "GB/s (amax + quantize passes)" if kind.startswith("quantize") else "GB/s",
                              "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    for kind in kernels:
+        kernels[kind]["traffic"] = ncu_traffic(kind)      # DRAM bytes per launch (ncu), or None
     dom = max(kinds.items(), key=lambda kv: kv[1][1])[0]
     n, tot_ms, units = kinds[dom]
     traffic = ncu_traffic(dom)
