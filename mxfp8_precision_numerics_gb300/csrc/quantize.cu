@@ -6,8 +6,9 @@
 //
 // Both kernels are HBM-bound streams. The amax pass reads the bf16 tensor once with
 // 16-byte loads and reduces |x| as integers (the magnitude order of non-NaN bf16 equals
-// the order of their low 15 bits). The quantize pass reads it again, 32 bytes (one 16-value
-// block) per thread, and writes 8 bytes of codes and 1 scale byte per block.
+// the order of their low 15 bits), sweeping the address range front to back. The quantize
+// pass reads it again back to front (so the part still in L2 is read first), 32 bytes (one
+// 16-value block) per thread, and writes 8 bytes of codes and 1 scale byte per block.
 #include "fp4q_common.cuh"
 #include "fp4q_internal.h"
 
@@ -15,7 +16,10 @@ namespace fp4q {
 
 // ---------------------------------------------------------------------------------------
 // amax over a [rows][ld] bf16 tensor (cols used per row), `batch` tensors along blockIdx.y.
-// Each warp takes whole rows; lanes stride over 16-byte vectors of the row.
+// The tensor is walked in 4 KB row segments (256 16-byte vectors), segment u by warp
+// u mod W in round u div W, so the segments in flight at any time are adjacent in memory and
+// the pass sweeps the address range once; the quantize pass then walks it backwards and
+// finds the most recently read part still in L2.
 // out[b] must be zero before the launch (atomicMax on the fp32 bit pattern).
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t* __restrict__ x,
@@ -24,28 +28,29 @@ __global__ void __launch_bounds__(256) amax_bf16_kernel(const uint16_t* __restri
                                                         float* __restrict__ out) {
     const uint16_t* base = x + (int64_t)blockIdx.y * batch_stride;
     const int64_t vecs = cols / 8;
+    const int64_t segs = (vecs + 255) / 256;
+    const int64_t units = rows * segs;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t warps_total = (int64_t)gridDim.x * 8;
     uint32_t m2 = 0;   // two packed |bf16| maxima
-    for (int64_t r = (int64_t)blockIdx.x * 8 + warp; r < rows; r += warps_total) {
+    for (int64_t u = (int64_t)blockIdx.x * 8 + warp; u < units; u += warps_total) {
+        const int64_t r = u / segs, sg = u - r * segs;
         const uint4* row = reinterpret_cast<const uint4*>(base + r * ld);
-        int64_t v = lane;
-        for (; v + 96 < vecs; v += 128) {
-            uint4 a = __ldg(row + v), b = __ldg(row + v + 32), c = __ldg(row + v + 64),
-                  d = __ldg(row + v + 96);
-            m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
-                                       __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
-            m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(b.x & 0x7FFF7FFFu, b.y & 0x7FFF7FFFu),
-                                       __vmaxu2(b.z & 0x7FFF7FFFu, b.w & 0x7FFF7FFFu)));
-            m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(c.x & 0x7FFF7FFFu, c.y & 0x7FFF7FFFu),
-                                       __vmaxu2(c.z & 0x7FFF7FFFu, c.w & 0x7FFF7FFFu)));
-            m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(d.x & 0x7FFF7FFFu, d.y & 0x7FFF7FFFu),
-                                       __vmaxu2(d.z & 0x7FFF7FFFu, d.w & 0x7FFF7FFFu)));
-        }
-        for (; v < vecs; v += 32) {
-            uint4 a = __ldg(row + v);
-            m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
-                                       __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
+        const int64_t v0 = sg * 256, v1 = v0 + 256 < vecs ? v0 + 256 : vecs;
+        if (v1 - v0 == 256) {
+            uint4 q[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) q[k] = __ldg(row + v0 + lane + 32 * k);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(q[k].x & 0x7FFF7FFFu, q[k].y & 0x7FFF7FFFu),
+                                           __vmaxu2(q[k].z & 0x7FFF7FFFu, q[k].w & 0x7FFF7FFFu)));
+        } else {
+            for (int64_t v = v0 + lane; v < v1; v += 32) {
+                uint4 a = __ldg(row + v);
+                m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
+                                           __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
+            }
         }
     }
     uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
@@ -118,7 +123,9 @@ __global__ void __launch_bounds__(256) quantize_1d_kernel(const uint16_t* __rest
     float s_enc, s_dec;
     global_scales(*amax_src, s_enc, s_dec);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < total; b += stride) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        // last rows first: they are the ones the amax pass read most recently, still in L2
+        const int64_t b = total - 1 - i;
         const int64_t r = b / nb, j = b - r * nb;
         const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + j * 16);
         uint4 p = __ldcs(src), q = __ldcs(src + 1);
@@ -132,11 +139,14 @@ __global__ void __launch_bounds__(256) quantize_1d_kernel(const uint16_t* __rest
 }
 
 // ---------------------------------------------------------------------------------------
-// 2D quantize: a CTA covers 16 rows x 256 columns (16 tiles of 16x16). Thread (r, t) loads
-// row r of tile t (32 contiguous bytes; 16 consecutive threads cover 512 contiguous bytes of
-// one row), the tile amax is reduced through shared memory, then each thread encodes its 16
-// values with the tile's scale. blockIdx.z = batch index (one tensor per expert).
+// 2D quantize: a CTA covers 16 rows x (256 kQ2Tiles) columns (16 kQ2Tiles tiles of 16x16).
+// Thread (r, t) loads row r of tiles t, t+16, ... (kQ2Tiles 32-byte loads in flight; 16
+// consecutive threads cover 512 contiguous bytes of one row per load), the tile amax is
+// reduced through shared memory, then each thread encodes its values with their tiles'
+// scales. blockIdx.z = batch index (one tensor per expert).
 // ---------------------------------------------------------------------------------------
+constexpr int kQ2Tiles = 2;
+
 template <bool kHwCvt>
 __global__ void __launch_bounds__(256) quantize_2d_kernel(const uint16_t* __restrict__ w,
                                                           int64_t rows, int64_t cols, int64_t ld,
@@ -148,31 +158,45 @@ __global__ void __launch_bounds__(256) quantize_2d_kernel(const uint16_t* __rest
     const int bz = blockIdx.z;
     const int r = threadIdx.x >> 4, t = threadIdx.x & 15;
     const int64_t tcols = cols >> 4;
-    const int64_t tile_c = (int64_t)blockIdx.x * 16 + t;
-    const int64_t row = (int64_t)blockIdx.y * 16 + r;
-    const bool valid = tile_c < tcols;
+    // last row strips first (the amax pass read them most recently; they are still in L2)
+    const int64_t by = (int64_t)gridDim.y - 1 - blockIdx.y;
+    const int64_t row = by * 16 + r;
     float s_enc, s_dec;
     global_scales(amax_src[bz], s_enc, s_dec);
-    uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (valid) {
-        const uint4* src = reinterpret_cast<const uint4*>(w + bz * batch_stride + row * ld + tile_c * 16);
-        uint4 p = __ldcs(src), q = __ldcs(src + 1);
-        v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w; v[4] = q.x; v[5] = q.y; v[6] = q.z; v[7] = q.w;
-    }
-    __shared__ float part[16][17];
-    part[r][t] = absmax16(v);
-    __syncthreads();
-    float amax_b = part[0][t];
+    uint32_t v[kQ2Tiles][8];
+    bool valid[kQ2Tiles];
 #pragma unroll
-    for (int i = 1; i < 16; ++i) amax_b = fmaxf(amax_b, part[i][t]);
-    if (valid) {
-        uint32_t sb = block_scale(amax_b, s_enc);
-        uint2 c = encode16<kHwCvt>(v, block_encode_scale(sb, s_dec));
-        uint8_t* crow = codes + bz * (rows * (cols >> 1)) + row * (cols >> 1);
-        reinterpret_cast<uint2*>(crow)[tile_c] = c;
-        if (r == 0) tile_scales[bz * ((rows >> 4) * tcols) + (int64_t)blockIdx.y * tcols + tile_c] = (uint8_t)sb;
+    for (int h = 0; h < kQ2Tiles; ++h) {
+        const int64_t tile_c = (int64_t)blockIdx.x * (16 * kQ2Tiles) + 16 * h + t;
+        valid[h] = tile_c < tcols;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[h][k] = 0;
+        if (valid[h]) {
+            const uint4* src = reinterpret_cast<const uint4*>(w + bz * batch_stride + row * ld + tile_c * 16);
+            uint4 p = __ldcs(src), q = __ldcs(src + 1);
+            v[h][0] = p.x; v[h][1] = p.y; v[h][2] = p.z; v[h][3] = p.w;
+            v[h][4] = q.x; v[h][5] = q.y; v[h][6] = q.z; v[h][7] = q.w;
+        }
     }
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) s_dec_out[bz] = s_dec;
+    __shared__ float part[kQ2Tiles][16][17];
+#pragma unroll
+    for (int h = 0; h < kQ2Tiles; ++h) part[h][r][t] = absmax16(v[h]);
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < kQ2Tiles; ++h) {
+        float amax_b = part[h][0][t];
+#pragma unroll
+        for (int i = 1; i < 16; ++i) amax_b = fmaxf(amax_b, part[h][i][t]);
+        if (valid[h]) {
+            const int64_t tile_c = (int64_t)blockIdx.x * (16 * kQ2Tiles) + 16 * h + t;
+            uint32_t sb = block_scale(amax_b, s_enc);
+            uint2 c = encode16<kHwCvt>(v[h], block_encode_scale(sb, s_dec));
+            uint8_t* crow = codes + bz * (rows * (cols >> 1)) + row * (cols >> 1);
+            reinterpret_cast<uint2*>(crow)[tile_c] = c;
+            if (r == 0) tile_scales[bz * ((rows >> 4) * tcols) + by * tcols + tile_c] = (uint8_t)sb;
+        }
+    }
+    if (blockIdx.x == 0 && by == 0 && threadIdx.x == 0) s_dec_out[bz] = s_dec;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -189,7 +213,8 @@ cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t l
                         int64_t batch_stride, float* out, cudaStream_t st) {
     cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * batch, st);
     if (e != cudaSuccess) return e;
-    int64_t g = (rows + 7) / 8;
+    const int64_t units = rows * ((cols / 8 + 255) / 256);
+    int64_t g = (units + 7) / 8;
     const int64_t cap = (int64_t)num_sms() * 8;
     if (g > cap) g = cap;
     amax_bf16_kernel<<<dim3((unsigned)g, (unsigned)batch), 256, 0, st>>>(x, rows, cols, ld,
@@ -213,7 +238,7 @@ cudaError_t launch_quantize_2d(const uint16_t* w, int64_t rows, int64_t cols, in
                                int64_t batch, int64_t batch_stride, const float* amax,
                                uint8_t* codes, uint8_t* tile_scales, float* s_dec,
                                cudaStream_t st) {
-    dim3 grid((unsigned)((cols / 16 + 15) / 16), (unsigned)(rows / 16), (unsigned)batch);
+    dim3 grid((unsigned)((cols / 16 + 16 * kQ2Tiles - 1) / (16 * kQ2Tiles)), (unsigned)(rows / 16), (unsigned)batch);
     if (use_hw_e2m1())
         quantize_2d_kernel<true><<<grid, 256, 0, st>>>(w, rows, cols, ld, batch_stride, amax, codes,
                                                        tile_scales, s_dec);
