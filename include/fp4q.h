@@ -217,6 +217,36 @@ FP4Q_API int fp4q_gemm_mxfp8(const uint8_t* a, const uint8_t* a_scales,
                     fp4q_stream_t stream);
 
 /*
+ * fp4q_gemm_nvfp4_gelu — fp4q_gemm_nvfp4 (groups == 1, bf16 output) with the MLP's activation
+ * fused into the epilogue: the first linear layer of a GPT MLP block, whose output feeds GELU
+ * and then the second layer's 1D NVFP4 quantization ([VZ] §13-14 pairs GELU with the quantize
+ * of its output). GELU is the exact-erf form x * Phi(x) evaluated in fp32 on the bf16 h.
+ *   h_out      [M][N] bf16 = the GEMM output (round to nearest even), as fp4q_gemm_nvfp4 writes it
+ *   act_out    [M][N] bf16 = GELU(h_out), round to nearest even
+ *   act_amax   device float: max |act_out| over the tensor, bit-exact, ready as the `amax_in`
+ *              of fp4q_quantize_1d(act_out) (which then skips its own amax pass)
+ *   Other arguments, shapes and alignment as fp4q_gemm_nvfp4 with groups == 1; h_out and
+ *   act_out 16-byte aligned.
+ */
+FP4Q_API int fp4q_gemm_nvfp4_gelu(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec,
+                    const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
+                    const float* b_s_dec, void* h_out, void* act_out, float* act_amax,
+                    int64_t M, int64_t N, int64_t K, fp4q_stream_t stream);
+
+/*
+ * fp4q_gemm_mxfp8_dgelu — fp4q_gemm_mxfp8 (bf16 output) with the activation's backward fused
+ * into the epilogue: the dgrad GEMM of the MLP's second layer produces dL/d(act); the
+ * epilogue rounds it to bf16 and multiplies by GELU'(h) = Phi(h) + h * phi(h) in fp32, giving
+ * dL/dh for the first layer's backward.
+ *   h          [M][N] bf16, the first layer's pre-activation (h_out of fp4q_gemm_nvfp4_gelu)
+ *   dh_out     [M][N] bf16 = bf16( bf16(A . B^T) * GELU'(h) ), round to nearest even
+ *   Other arguments, shapes and alignment as fp4q_gemm_mxfp8; h and dh_out 16-byte aligned.
+ */
+FP4Q_API int fp4q_gemm_mxfp8_dgelu(const uint8_t* a, const uint8_t* a_scales,
+                    const uint8_t* b, const uint8_t* b_scales, const void* h, void* dh_out,
+                    int64_t M, int64_t N, int64_t K, fp4q_stream_t stream);
+
+/*
  * fp4q_device_status — synchronizes `stream`, then reads and clears the library's device-side
  * error word. Returns FP4Q_ERR_TIMEOUT if a kernel's bounded wait (a GEMM pipeline barrier)
  * gave up since the last call, FP4Q_ERR_CUDA if the stream reports an error, else FP4Q_OK.

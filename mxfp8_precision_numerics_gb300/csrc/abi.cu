@@ -227,6 +227,72 @@ int fp4q_gemm_mxfp8(const uint8_t* a, const uint8_t* a_scales,
     return cuda_status(fp4q::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int fp4q_gemm_nvfp4_gelu(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec,
+                         const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
+                         const float* b_s_dec, void* h_out, void* act_out, float* act_amax,
+                         int64_t M, int64_t N, int64_t K, fp4q_stream_t stream) {
+    if (b_scale_kind != FP4Q_SCALE_1D && b_scale_kind != FP4Q_SCALE_2D) return FP4Q_ERR_ARG;
+    if (!a || !a_scales || !a_s_dec || !b || !b_scales || !b_s_dec || !h_out || !act_out || !act_amax)
+        return FP4Q_ERR_NULL;
+    if (M < 1 || N < 16 || N % 16 != 0 || K < 256 || K % 256 != 0) return FP4Q_ERR_SHAPE;
+    if (M > 2147483647 || N > 2147483647) return FP4Q_ERR_SHAPE;
+    if (b_scale_kind == FP4Q_SCALE_2D && N % 16 != 0) return FP4Q_ERR_SHAPE;
+    if (!al16(a) || !al16(b) || !al16(a_scales) || !al16(b_scales) || !al16(h_out) || !al16(act_out))
+        return FP4Q_ERR_ALIGN;
+    if (!al4(act_amax)) return FP4Q_ERR_ALIGN;
+    if (int d = check_device()) return d;
+    fp4q::GemmArgs g;
+    g.kind = 0;
+    g.a = a;
+    g.a_scales = a_scales;
+    g.a_s_dec = a_s_dec;
+    g.b = b;
+    g.b_scales = b_scales;
+    g.b_scale_kind = b_scale_kind;
+    g.b_s_dec = b_s_dec;
+    g.d = h_out;
+    g.d_bf16 = 1;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.groups = 1;
+    g.group_offsets = nullptr;
+    g.epi = 1;
+    g.d2 = act_out;
+    g.amax_out = act_amax;
+    return cuda_status(fp4q::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp4q_gemm_mxfp8_dgelu(const uint8_t* a, const uint8_t* a_scales,
+                          const uint8_t* b, const uint8_t* b_scales, const void* h, void* dh_out,
+                          int64_t M, int64_t N, int64_t K, fp4q_stream_t stream) {
+    if (!a || !a_scales || !b || !b_scales || !h || !dh_out) return FP4Q_ERR_NULL;
+    if (M < 1 || N < 16 || N % 16 != 0 || K < 128 || K % 128 != 0) return FP4Q_ERR_SHAPE;
+    if (M > 2147483647 || N > 2147483647) return FP4Q_ERR_SHAPE;
+    if (!al16(a) || !al16(b) || !al4(a_scales) || !al4(b_scales) || !al16(h) || !al16(dh_out))
+        return FP4Q_ERR_ALIGN;
+    if (int dv = check_device()) return dv;
+    fp4q::GemmArgs g;
+    g.kind = 1;
+    g.a = a;
+    g.a_scales = a_scales;
+    g.a_s_dec = nullptr;
+    g.b = b;
+    g.b_scales = b_scales;
+    g.b_scale_kind = 1;
+    g.b_s_dec = nullptr;
+    g.d = dh_out;
+    g.d_bf16 = 1;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.groups = 1;
+    g.group_offsets = nullptr;
+    g.epi = 2;
+    g.aux = static_cast<const uint16_t*>(h);
+    return cuda_status(fp4q::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fp4q_device_status(fp4q_stream_t stream) {
     int flag = 0;
     if (fp4q::read_and_clear_device_error(reinterpret_cast<cudaStream_t>(stream), &flag) != 0)

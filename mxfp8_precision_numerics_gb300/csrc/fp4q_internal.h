@@ -50,6 +50,12 @@ struct GemmArgs {
     int64_t M, N, K;
     int groups;
     const int64_t* group_offsets;   // host, groups + 1 (NULL when groups == 1)
+    // epilogue (bf16 output only): 0 plain; 1 GELU: d = h, d2 = GELU(h), amax_out = max|d2|;
+    // 2 GELU backward: d = bf16(d_bf16 * GELU'(aux)), aux = the layer's pre-activation h
+    int epi = 0;
+    void* d2 = nullptr;
+    const uint16_t* aux = nullptr;
+    float* amax_out = nullptr;
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st);
 int read_and_clear_device_error(cudaStream_t st, int* flag);

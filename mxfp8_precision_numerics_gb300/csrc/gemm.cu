@@ -91,6 +91,10 @@ struct Params {
     int groups;
     int64_t goff[65];
     int gtile[65];
+    int epi;                   // 0 plain, 1 GELU (d = h, d2 = GELU(h), amax), 2 GELU backward
+    void* d2;
+    const uint16_t* aux;
+    float* amax_out;
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -224,46 +228,147 @@ constexpr uint32_t kIdescNvfp4 = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) 
 constexpr uint32_t kIdescMxfp8 = (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                                  (1u << 23) | ((uint32_t)(kBM >> 4) << 24);
 
+// ------------------------------------------------------------------ bf16 epilogues
+// GELU in its exact-erf form, x * Phi(x) ("Gaussian Error Linear Units", Hendrycks & Gimpel),
+// and its derivative Phi(x) + x * phi(x). Phi comes from erfc's Chebyshev fit (Numerical
+// Recipes, 2nd ed., §6.2, erfcc; fractional error below 1.2e-7 everywhere) evaluated on
+// z = |x| / sqrt(2), Phi(x) = erfc(-x / sqrt(2)) / 2, so neither tail suffers cancellation;
+// exp and the reciprocal use the approximate hardware units (the result is rounded to bf16).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ void norm_cdf_pdf(float x, float& cdf, float& pdf) {
+    const float kLog2e = 1.4426950408889634f;
+    const float z = __fmul_rn(fabsf(x), 0.70710678118654752f);
+    const float t = rcp_approx(__fmaf_rn(0.5f, z, 1.0f));
+    float q = 0.17087277f;
+    q = __fmaf_rn(q, t, -0.82215223f);
+    q = __fmaf_rn(q, t, 1.48851587f);
+    q = __fmaf_rn(q, t, -1.13520398f);
+    q = __fmaf_rn(q, t, 0.27886807f);
+    q = __fmaf_rn(q, t, -0.18628806f);
+    q = __fmaf_rn(q, t, 0.09678418f);
+    q = __fmaf_rn(q, t, 0.37409196f);
+    q = __fmaf_rn(q, t, 1.00002368f);
+    q = __fmaf_rn(q, t, -1.26551223f);
+    const float zz = __fmul_rn(z, z);
+    const float erfc_z = __fmul_rn(t, ex2_approx(__fmul_rn(__fsub_rn(q, zz), kLog2e)));
+    cdf = x >= 0.0f ? __fmaf_rn(-0.5f, erfc_z, 1.0f) : __fmul_rn(0.5f, erfc_z);
+    pdf = __fmul_rn(ex2_approx(__fmul_rn(-zz, kLog2e)), 0.39894228040143268f);   // e^(-x^2/2)/sqrt(2 pi)
+}
+__device__ __forceinline__ float gelu_f(float x) {
+    float cdf, pdf;
+    norm_cdf_pdf(x, cdf, pdf);
+    return __fmul_rn(x, cdf);
+}
+__device__ __forceinline__ float gelu_grad_f(float x) {
+    float cdf, pdf;
+    norm_cdf_pdf(x, cdf, pdf);
+    return __fmaf_rn(x, pdf, cdf);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h2);
+}
+// 32 accumulator columns (raw fp32 bits) x alpha -> 16 packed bf16 pairs
+__device__ __forceinline__ void pack_chunk(const uint32_t (&r)[32], float alpha, uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        pk[i] = pack_bf16x2(__fmul_rn(__uint_as_float(r[2 * i]), alpha), __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
+}
+__device__ __forceinline__ void store_packed(void* base, int64_t row, int64_t N, int64_t col, const uint32_t (&pk)[16],
+                                             bool full32) {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + row * N + col);
+    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    if (full32) {
+        dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+        dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+    }
+}
+// One row's 32 bf16 output columns (pk = bf16(acc x alpha)) through the epilogue p.epi.
+// amax_bits: running max of |GELU(h)| as bf16 magnitude bits (epi 1).
+__device__ __forceinline__ void epi_bf16(const Params& p, const uint32_t (&pk)[16], int64_t row, bool row_ok,
+                                         int64_t col, uint32_t& amax_bits) {
+    if (!row_ok || col >= p.N) return;
+    const bool full32 = col + 32 <= p.N;      // N % 16 == 0: a partial chunk has 16 columns
+    if (p.epi == 2) {
+        const uint4* hs = reinterpret_cast<const uint4*>(p.aux + row * p.N + col);
+        uint32_t hw[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 v = (q < 2 || full32) ? __ldcs(hs + q) : make_uint4(0, 0, 0, 0);
+            hw[4 * q] = v.x; hw[4 * q + 1] = v.y; hw[4 * q + 2] = v.z; hw[4 * q + 3] = v.w;
+        }
+        uint32_t o[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(pk[i] << 16), g1 = __uint_as_float(pk[i] & 0xFFFF0000u);
+            const float h0 = __uint_as_float(hw[i] << 16), h1 = __uint_as_float(hw[i] & 0xFFFF0000u);
+            o[i] = pack_bf16x2(__fmul_rn(g0, gelu_grad_f(h0)), __fmul_rn(g1, gelu_grad_f(h1)));
+        }
+        store_packed(p.d, row, p.N, col, o, full32);
+        return;
+    }
+    store_packed(p.d, row, p.N, col, pk, full32);
+    if (p.epi == 1) {
+        uint32_t o[16];
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            o[i] = pack_bf16x2(gelu_f(__uint_as_float(pk[i] << 16)), gelu_f(__uint_as_float(pk[i] & 0xFFFF0000u)));
+            if (i < 8 || full32) m2 = __vmaxu2(m2, o[i] & 0x7FFF7FFFu);
+        }
+        amax_bits = max(amax_bits, max(m2 & 0xFFFFu, m2 >> 16));
+        store_packed(p.d2, row, p.N, col, o, full32);
+    }
+}
+// The warp's running |GELU| max into amax_out (fp32 bit pattern of the bf16 magnitude).
+__device__ __forceinline__ void epi_flush_amax(const Params& p, uint32_t amax_bits, int lane) {
+    if (p.epi != 1) return;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, o));
+    if (lane == 0 && amax_bits) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), amax_bits << 16);
+}
+
 // Epilogue of one 128 x 256 accumulator: warp w (TMEM lane quarter w) loads rows
 // m0 + 32w + lane, 32 columns at a time, scales by alpha and stores fp32 or bf16.
 __device__ __forceinline__ void store_tile(const Params& p, uint32_t tacc, int warp, int lane, int64_t m0,
                                            int64_t m_end, int64_t n0, float alpha) {
     const int64_t row = m0 + warp * 32 + lane;
     const bool row_ok = row < m_end;
+    uint32_t amax_bits = 0;
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(tacc + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
         const int64_t col = n0 + c * 32;
-        if (!row_ok || col >= p.N) continue;
-        const bool full32 = col + 32 <= p.N;
         if (p.d_bf16) {
             uint32_t pk[16];
+            pack_chunk(r, alpha, pk);
+            epi_bf16(p, pk, row, row_ok, col, amax_bits);
+            continue;
+        }
+        if (!row_ok || col >= p.N) continue;
+        const bool full32 = col + 32 <= p.N;
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.N + col);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha),
-                                                          __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
-                pk[i] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + row * p.N + col);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            if (full32) {
-                dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-                dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
-            }
-        } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.N + col);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (i >= 4 && !full32) break;
-                dst[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
-                                     __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
-                                     __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
-                                     __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
-            }
+        for (int i = 0; i < 8; ++i) {
+            if (i >= 4 && !full32) break;
+            dst[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
         }
     }
+    epi_flush_amax(p, amax_bits, lane);
 }
 
 // Scale writer step (warps 0-3): copy one stage's staged scale rows into tensor memory in the
@@ -591,8 +696,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 //     own tensor memory, then an arrival on the leader's `sf_ready` barrier (8 arrivals).
 //   MMA issuer (warp 5 lane 0, leader only): waits for tensor memory to be free of the previous
 //     tile (`tmem_empty`), then 4 MMAs per K-block; commits are multicast to both CTAs.
-//   epilogue (warps 6-13, each CTA): copies its accumulator slice to registers, releases the
-//     tensor memory, then scales and stores while the next tile's MMAs run.
+//   epilogue (warps 6-13, each CTA): copies its accumulator slice (128 columns) to registers
+//     (bf16 outputs rounded to bf16 pairs on the way), releases the tensor memory, then runs
+//     the epilogue (plain, GELU or GELU backward) and stores while the next tile's MMAs run.
 // Pipeline depths of the pair kernel.
 //   S   A/B stages in shared memory (TMA, counted on the leader's `full` barrier)
 //   G   K-blocks per scale unit: one TMA box per operand holds the scales of G K-blocks for
@@ -702,36 +808,19 @@ __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32
                  : "r"(taddr) : "memory");
 }
 
-// One row's 32 accumulator columns, scaled by alpha, stored as fp32 or bf16.
+// One row's 32 accumulator columns, scaled by alpha, stored as fp32.
 __device__ __forceinline__ void store_chunk(const Params& p, const uint32_t (&r)[32], int64_t row, bool row_ok,
                                             int64_t col, float alpha) {
     if (!row_ok || col >= p.N) return;
     const bool full32 = col + 32 <= p.N;
-    if (p.d_bf16) {
-        uint32_t pk[16];
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.N + col);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha),
-                                                      __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
-            pk[i] = *reinterpret_cast<uint32_t*>(&h2);
-        }
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.d) + row * p.N + col);
-        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        if (full32) {
-            dst[2] = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-            dst[3] = make_uint4(pk[12], pk[13], pk[14], pk[15]);
-        }
-    } else {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.N + col);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (i >= 4 && !full32) break;
-            dst[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
-                                 __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
-                                 __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
-                                 __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
-        }
+    for (int i = 0; i < 8; ++i) {
+        if (i >= 4 && !full32) break;
+        dst[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
+                             __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
+                             __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
+                             __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
     }
 }
 
@@ -754,7 +843,7 @@ __device__ __forceinline__ void pair_tile(const Params& p, int tile, uint32_t ra
 // tensor-memory lane quarter, 128 accumulator columns each). The epilogue copies the finished
 // accumulator to registers, releases it (tmem_empty) and stores while the next tile's MMAs run;
 // the producer and the writers run ahead into the next tile meanwhile.
-constexpr int kPairThreads = 448;
+constexpr int kPairThreads = 448;   // 6 + 8 warps
 
 template <int kKind>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
@@ -938,10 +1027,12 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         }
     } else {
         // ------------------------------------------------ warps 6-13: epilogue
-        const int q = warp & 3, h = (warp - 6) >> 2;          // lane quarter, column half
+        // two warps per tensor-memory lane quarter (the quarter is warp mod 4), 128 columns each
+        const int q = warp & 3, h = (warp - 6) >> 2;
         const uint32_t tacc = tmem + kAccCol + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
         const uint32_t empty_leader = leader_addr(tmem_empty);
         const float alpha = kKind == 0 ? __fmul_rn(p.a_s_dec[0], p.b_s_dec[0]) : 1.0f;
+        uint32_t amax_bits = 0;
         for (int ti = 0; ti < my_tiles; ++ti) {
             int64_t m0, n0;
             pair_tile(p, cid + ti * ncl, rank, m0, n0);
@@ -950,28 +1041,31 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
             const int64_t row = m0 + 32 * q + lane;
             const bool row_ok = row < p.M;
             const int64_t col0 = n0 + 128 * h;
-            if (kKind == 1) {
-                // MXFP8: the slice's 128 columns into registers with one wait, tensor memory back
-                // to the MMAs, then scale and store
-                uint32_t r0[32], r1[32], r2[32], r3[32];
-                tmem_ld32_async(tacc, r0);
-                tmem_ld32_async(tacc + 32, r1);
-                tmem_ld32_async(tacc + 64, r2);
-                tmem_ld32_async(tacc + 96, r3);
-                tmem_wait_ld(r0);
-                tmem_wait_ld(r1);
-                tmem_wait_ld(r2);
-                tmem_wait_ld(r3);
+            if (p.d_bf16) {
+                // bf16 output: each 32-column chunk is rounded to bf16 pairs as soon as it is in
+                // registers (64 registers for the slice), tensor memory goes back to the MMAs,
+                // then the epilogue and the stores
+                uint32_t pk[4][16];
+                uint32_t ra[32], rb[32];
+                tmem_ld32_async(tacc, ra);
+                tmem_ld32_async(tacc + 32, rb);
+                tmem_wait_ld(ra);
+                pack_chunk(ra, alpha, pk[0]);
+                tmem_ld32_async(tacc + 64, ra);
+                tmem_wait_ld(rb);
+                pack_chunk(rb, alpha, pk[1]);
+                tmem_ld32_async(tacc + 96, rb);
+                tmem_wait_ld(ra);
+                pack_chunk(ra, alpha, pk[2]);
+                tmem_wait_ld(rb);
+                pack_chunk(rb, alpha, pk[3]);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_leader);
-                store_chunk(p, r0, row, row_ok, col0, alpha);
-                store_chunk(p, r1, row, row_ok, col0 + 32, alpha);
-                store_chunk(p, r2, row, row_ok, col0 + 64, alpha);
-                store_chunk(p, r3, row, row_ok, col0 + 96, alpha);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) epi_bf16(p, pk[c], row, row_ok, col0 + 32 * c, amax_bits);
             } else {
-                // NVFP4: loads interleaved with the stores of the previous chunk, so that most of
-                // the output traffic is out before the next tile's operand stream restarts
+                // fp32 output: loads interleaved with the stores of the previous chunk
                 uint32_t ra[32], rb[32];
                 tmem_ld32_async(tacc, ra);
                 tmem_wait_ld(ra);
@@ -990,6 +1084,7 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
                 store_chunk(p, rb, row, row_ok, col0 + 96, alpha);
             }
         }
+        epi_flush_amax(p, amax_bits, lane);
     }
 
     tc_fence_before();
@@ -1069,6 +1164,10 @@ cudaError_t launch_kind(const GemmArgs& a, cudaStream_t st) {
     p.b_s_dec = a.b_s_dec;
     p.d = a.d;
     p.d_bf16 = a.d_bf16;
+    p.epi = a.epi;
+    p.d2 = a.d2;
+    p.aux = a.aux;
+    p.amax_out = a.amax_out;
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;
@@ -1127,6 +1226,10 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
     p.b_s_dec = a.b_s_dec;
     p.d = a.d;
     p.d_bf16 = a.d_bf16;
+    p.epi = a.epi;
+    p.d2 = a.d2;
+    p.aux = a.aux;
+    p.amax_out = a.amax_out;
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;
@@ -1168,6 +1271,10 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
 #define FP4Q_PAIR_MIN_STAGES 1
 #endif
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
+    if (a.epi == 1) {   // the epilogue's |GELU| maximum is an atomicMax into a zeroed word
+        const cudaError_t e = cudaMemsetAsync(a.amax_out, 0, sizeof(float), st);
+        if (e != cudaSuccess) return e;
+    }
     const int64_t stages = a.K / (a.kind == 0 ? Cfg<0>::kValuesPerStage : Cfg<1>::kValuesPerStage);
     // the pair kernel's scale TMA wants 16-byte aligned scale rows
     const int64_t sc_ld = a.kind == 0 ? a.K / 16 : a.K / 32;

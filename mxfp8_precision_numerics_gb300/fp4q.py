@@ -53,6 +53,8 @@ _SIGS = {
     "fp4q_gemm_nvfp4": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _int, _i64, _i64, _i64, _int,
                                ctypes.POINTER(ctypes.c_int64), _vp]),
     "fp4q_gemm_mxfp8": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp]),
+    "fp4q_gemm_nvfp4_gelu": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "fp4q_gemm_mxfp8_dgelu": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "fp4q_device_status": (_int, [_vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -140,6 +142,18 @@ def fp4q_gemm_mxfp8(a, a_scales, b, b_scales, d, d_dtype, M, N, K, stream=None):
                                 M, N, K, _stream(stream)), "fp4q_gemm_mxfp8")
 
 
+def fp4q_gemm_nvfp4_gelu(a, a_scales, a_s_dec, b, b_scales, b_scale_kind, b_s_dec, h_out, act_out, act_amax,
+                         M, N, K, stream=None):
+    _check(_lib.fp4q_gemm_nvfp4_gelu(_ptr(a), _ptr(a_scales), _ptr(a_s_dec), _ptr(b), _ptr(b_scales),
+                                     b_scale_kind, _ptr(b_s_dec), _ptr(h_out), _ptr(act_out), _ptr(act_amax),
+                                     M, N, K, _stream(stream)), "fp4q_gemm_nvfp4_gelu")
+
+
+def fp4q_gemm_mxfp8_dgelu(a, a_scales, b, b_scales, h, dh_out, M, N, K, stream=None):
+    _check(_lib.fp4q_gemm_mxfp8_dgelu(_ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), _ptr(h), _ptr(dh_out),
+                                      M, N, K, _stream(stream)), "fp4q_gemm_mxfp8_dgelu")
+
+
 def fp4q_device_status(stream=None):
     return _lib.fp4q_device_status(_stream(stream))
 
@@ -207,6 +221,26 @@ def gemm_nvfp4(a, a_scales, a_s_dec, b, b_scales, b_scale_kind, b_s_dec, out_dty
                     BF16 if out_dtype == torch.bfloat16 else F32, M, N, K, groups, group_row_offsets,
                     stream)
     return d
+
+
+def gemm_nvfp4_gelu(a, a_scales, a_s_dec, b, b_scales, b_scale_kind, b_s_dec, stream=None):
+    """-> (h, act, act_amax): h = A.B^T in bf16, act = GELU(h) in bf16, act_amax = max|act|."""
+    M, K = a.shape[0], a.shape[1] * 2
+    N = b.shape[-2]
+    h = _empty((M, N), torch.bfloat16, a.device)
+    act = _empty((M, N), torch.bfloat16, a.device)
+    amax = _empty((1,), torch.float32, a.device)
+    fp4q_gemm_nvfp4_gelu(a, a_scales, a_s_dec, b, b_scales, b_scale_kind, b_s_dec, h, act, amax, M, N, K, stream)
+    return h, act, amax
+
+
+def gemm_mxfp8_dgelu(a, a_scales, b, b_scales, h, stream=None):
+    """-> dh = bf16(bf16(A.B^T) * GELU'(h)), bf16 [M][N]."""
+    M, K = a.shape
+    N = b.shape[0]
+    dh = _empty((M, N), torch.bfloat16, a.device)
+    fp4q_gemm_mxfp8_dgelu(a, a_scales, b, b_scales, h, dh, M, N, K, stream)
+    return dh
 
 
 def gemm_mxfp8(a, a_scales, b, b_scales, out_dtype=torch.float32, stream=None):

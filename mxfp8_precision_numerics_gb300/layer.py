@@ -9,9 +9,11 @@ as it is for dgrad and transposed (with the 16-point RHT) for wgrad; the saved N
 weight and activation are dequantized, transposed and re-quantized to MXFP8 with SR
 (the activation with the RHT, the weight without). dgrad sums over N, wgrad over tokens.
 
-GELU and its derivative between the two linear layers of the MLP block run in PyTorch
-(bf16, exact erf form): they are the block's glue, not part of the quantized path.
-Every quantize, requantize, transform and GEMM runs in libfp4q.
+GELU between the two linear layers of the MLP block (exact erf form, bf16) is fused into the
+epilogues of the GEMMs around it: the first layer's NVFP4 GEMM writes h, GELU(h) and
+max|GELU(h)| (which the second layer's quantize takes as its amax), and the second layer's
+dgrad GEMM multiplies by GELU'(h) before writing dL/dh. Every quantize, requantize, transform,
+GEMM and activation runs in libfp4q.
 """
 from dataclasses import dataclass
 
@@ -29,29 +31,38 @@ class SavedLinear:
     N: int
 
 
-def linear_forward(x, w=None, wq=None, out_dtype=torch.bfloat16, stream=None):
-    """y = x w^T on NVFP4 operands. x: [M, K] bf16; w: [N, K] bf16 (or wq precomputed)."""
+def linear_forward(x, w=None, wq=None, out_dtype=torch.bfloat16, stream=None, x_amax=None, gelu=False):
+    """y = x w^T on NVFP4 operands. x: [M, K] bf16; w: [N, K] bf16 (or wq precomputed).
+    x_amax: max|x| if already known (device float), else the quantizer computes it.
+    gelu=True returns ((h, GELU(h), max|GELU(h)|), saved) instead of (y, saved)."""
     M, K = x.shape
-    xc, xs, xsd, _ = F.quantize_1d(x, stream=stream)
+    xc, xs, xsd, _ = F.quantize_1d(x, amax_in=x_amax, stream=stream)
     if wq is None:
         wc, ws, wsd, _ = F.quantize_2d(w, stream=stream)
         wq = (wc, ws, wsd)
     wc, ws, wsd = wq
     N = wc.shape[0]
+    saved = SavedLinear((xc, xs, xsd), wq, M, K, N)
+    if gelu:
+        return F.gemm_nvfp4_gelu(xc, xs, xsd, wc, ws, F.SCALE_2D, wsd, stream=stream), saved
     y = F.gemm_nvfp4(xc, xs, xsd, wc, ws, F.SCALE_2D, wsd, out_dtype, stream=stream)
-    return y, SavedLinear((xc, xs, xsd), wq, M, K, N)
+    return y, saved
 
 
 def linear_backward(dy, saved, seed, rht_signs, dx_dtype=torch.bfloat16, stream=None,
-                    rounding=F.SR):
-    """dy: [M, N] bf16 -> (dx [M, K], dw [N, K] fp32)."""
+                    rounding=F.SR, dgelu_h=None):
+    """dy: [M, N] bf16 -> (dx [M, K], dw [N, K] fp32). dgelu_h: the previous layer's
+    pre-activation h; when given, dx is returned as dx * GELU'(h) (bf16)."""
     M, K, N = saved.M, saved.K, saved.N
     xc, xs, xsd = saved.xq
     wc, ws, wsd = saved.wq
     # dgrad: dx[m, k] = sum_n dy[m, n] w[n, k]   (blocks along N on both operands)
     g = F.requant_mxfp8(F.IN_BF16, dy, None, None, M, N, 0, 0, 0, rounding, seed, F.TAG_DY_ROWS, stream)
     wt = F.requant_mxfp8(F.IN_NVFP4_2D, wc, ws, wsd, N, K, 1, 0, 0, rounding, seed, F.TAG_WT, stream)
-    dx = F.gemm_mxfp8(g[0], g[1], wt[0], wt[1], dx_dtype, stream)
+    if dgelu_h is not None:
+        dx = F.gemm_mxfp8_dgelu(g[0], g[1], wt[0], wt[1], dgelu_h, stream)
+    else:
+        dx = F.gemm_mxfp8(g[0], g[1], wt[0], wt[1], dx_dtype, stream)
     # wgrad: dw[n, k] = sum_m dy[m, n] x[m, k]   (blocks and RHT along tokens)
     gt = F.requant_mxfp8(F.IN_BF16, dy, None, None, M, N, 1, 1, rht_signs, rounding, seed, F.TAG_DY_T, stream)
     xt = F.requant_mxfp8(F.IN_NVFP4_1D, xc, xs, xsd, M, K, 1, 1, rht_signs, rounding, seed, F.TAG_XT, stream)
@@ -61,16 +72,15 @@ def linear_backward(dy, saved, seed, rht_signs, dx_dtype=torch.bfloat16, stream=
 
 def mlp_forward(x, w1, w2, stream=None):
     """GPT MLP block: y = gelu(x w1^T) w2^T. x [M, D], w1 [Fh, D], w2 [D, Fh]."""
-    h, s1 = linear_forward(x, w1, stream=stream)
-    a = torch.nn.functional.gelu(h)
-    y, s2 = linear_forward(a, w2, stream=stream)
+    (h, a, a_amax), s1 = linear_forward(x, w1, stream=stream, gelu=True)
+    y, s2 = linear_forward(a, w2, stream=stream, x_amax=a_amax)
     return y, (h, s1, s2)
 
 
 def mlp_backward(dy, saved, seed, rht_signs, stream=None):
     h, s1, s2 = saved
-    da, dw2 = linear_backward(dy, s2, seed, rht_signs, stream=stream)
-    dh = torch.ops.aten.gelu_backward(da, h)
+    # layer 2's dgrad GEMM applies GELU'(h): dh = (dy w2) * GELU'(h)
+    dh, dw2 = linear_backward(dy, s2, seed, rht_signs, stream=stream, dgelu_h=h)
     # a second layer draws from its own counter stream: offset the seed
     dx, dw1 = linear_backward(dh, s1, seed ^ 0x9E3779B97F4A7C15, rht_signs, stream=stream)
     return dx, dw1, dw2
@@ -83,6 +93,7 @@ def mlp_gemm_flops(M, D, Fh):
 
 def mlp_kernel_launches():
     """libfp4q kernels one mlp_forward + mlp_backward launches (counted from the calls):
-    forward: 2 x (amax + quantize_1d, amax + quantize_2d, NVFP4 GEMM) = 10;
-    backward: 2 x (4 requant + 2 MXFP8 GEMM) = 12."""
-    return 22
+    forward: amax + quantize_1d of x, quantize_1d of GELU(h) (its amax comes from the GELU
+    GEMM's epilogue), 2 x (amax + quantize_2d of a weight), 2 NVFP4 GEMMs = 9;
+    backward: 2 x (4 requant + 2 MXFP8 GEMMs) = 12."""
+    return 21

@@ -95,6 +95,17 @@ def test_validation_rejects_bad_arguments_without_touching_cuda(F):
     assert m(p, p, p, p, p, 0, 128, 256, 96, n) == F.ERR_SHAPE
     assert m(p, p, p, p, n, 0, 128, 256, 128, n) == F.ERR_NULL
     assert m(p, ctypes.c_void_p(18), p, p, p, 0, 128, 256, 128, n) == F.ERR_ALIGN
+    # the fused-epilogue GEMMs
+    ge = L.fp4q_gemm_nvfp4_gelu
+    assert ge(p, p, p, p, p, 2, p, p, n, p, 128, 256, 256, n) == F.ERR_NULL           # no act_out
+    assert ge(p, p, p, p, p, 2, p, p, p, n, 128, 256, 256, n) == F.ERR_NULL           # no amax
+    assert ge(p, p, p, p, p, 3, p, p, p, p, 128, 256, 256, n) == F.ERR_ARG            # scale kind
+    assert ge(p, p, p, p, p, 2, p, p, p, p, 128, 256, 200, n) == F.ERR_SHAPE          # K % 256
+    assert ge(p, p, p, p, p, 2, p, p, q, p, 128, 256, 256, n) == F.ERR_ALIGN          # h_out
+    dg = L.fp4q_gemm_mxfp8_dgelu
+    assert dg(p, p, p, p, n, p, 128, 256, 128, n) == F.ERR_NULL                        # no h
+    assert dg(p, p, p, p, p, p, 128, 250, 128, n) == F.ERR_SHAPE                       # N % 16
+    assert dg(p, p, p, p, p, q, 128, 256, 128, n) == F.ERR_ALIGN                       # dh_out
 
 
 def test_product_path_has_no_oracle_or_fallback():
