@@ -171,6 +171,29 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b,
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
                  ::"r"(taddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+// tcgen05.st of 8 / 16 / 32 consecutive columns (one 32-bit register per column and lane)
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                   "r"(v[7]) : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11,"
+                 " %12, %13, %14, %15, %16};"
+                 ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                   "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+                   "r"(v[15]) : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11,"
+                 " %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29,"
+                 " %30, %31, %32};"
+                 ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                   "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+                   "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+                   "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+                   "r"(v[29]), "r"(v[30]), "r"(v[31]) : "memory");
+}
 // cp.async of `bytes` (4 or 16) with zero fill when `valid` is false
 template <int kBytes>
 __device__ __forceinline__ void cp_async_zfill(uint32_t dst, const void* src, bool valid) {
@@ -749,37 +772,45 @@ __device__ __forceinline__ void write_unit_scales(const uint8_t* unit, int sub, 
     constexpr uint32_t W = sf_unit_w<kKind>();
     const uint8_t* ua = unit + sub * Cfg<kKind>::kSfRowBytes;
     const uint8_t* ub = unit + sf_unit_a<kKind>() + sub * Cfg<kKind>::kSfRowBytes;
+    static_assert(kKind != 0 || W == 64, "the NVFP4 swizzle below assumes 64-byte scale rows");
     if (kKind == 0) {
+        // NVFP4 units arrive with the TMA's 64-byte swizzle: the 16-byte chunk `sub` of row r
+        // sits at chunk sub ^ ((r >> 1) & 3), so the 8 lanes of a quarter-warp read 8 distinct
+        // bank groups (with plain 64-byte rows they collided 4 ways)
+        const uint8_t* a0 = unit;
+        const uint8_t* b0 = unit + sf_unit_a<kKind>();
         uint4 a[4], b[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint4*>(ua + (lane + 32 * c) * W);
+        for (int c = 0; c < 4; ++c) {
+            const int r = lane + 32 * c;
+            a[c] = *reinterpret_cast<const uint4*>(a0 + r * W + 16 * (sub ^ ((r >> 1) & 3)));
+        }
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            const int r = lane + 32 * c;
-            b[c] = *reinterpret_cast<const uint4*>(ub + (b2d ? (r >> 4) : r) * W);
+            const int r = b2d ? ((lane + 32 * c) >> 4) : lane + 32 * c;
+            b[c] = *reinterpret_cast<const uint4*>(b0 + r * W + 16 * (sub ^ ((r >> 1) & 3)));
         }
-        // MMA j: SFA in columns sf + 4j + c, SFB in columns sf + 16 + 8j + c
-        tmem_st4(sf + 0, a[0].x, a[1].x, a[2].x, a[3].x);
-        tmem_st4(sf + 4, a[0].y, a[1].y, a[2].y, a[3].y);
-        tmem_st4(sf + 8, a[0].z, a[1].z, a[2].z, a[3].z);
-        tmem_st4(sf + 12, a[0].w, a[1].w, a[2].w, a[3].w);
-        tmem_st4(sf + 16, b[0].x, b[1].x, b[2].x, b[3].x);
-        tmem_st4(sf + 20, b[4].x, b[5].x, b[6].x, b[7].x);
-        tmem_st4(sf + 24, b[0].y, b[1].y, b[2].y, b[3].y);
-        tmem_st4(sf + 28, b[4].y, b[5].y, b[6].y, b[7].y);
-        tmem_st4(sf + 32, b[0].z, b[1].z, b[2].z, b[3].z);
-        tmem_st4(sf + 36, b[4].z, b[5].z, b[6].z, b[7].z);
-        tmem_st4(sf + 40, b[0].w, b[1].w, b[2].w, b[3].w);
-        tmem_st4(sf + 44, b[4].w, b[5].w, b[6].w, b[7].w);
+        // MMA j: SFA in columns sf + 4j + c (c = row / 32), SFB in columns sf + 16 + 8j + c;
+        // the 16 SFA and 32 SFB columns are consecutive: one x16 and one x32 store
+        const uint32_t va[16] = {a[0].x, a[1].x, a[2].x, a[3].x, a[0].y, a[1].y, a[2].y, a[3].y,
+                                 a[0].z, a[1].z, a[2].z, a[3].z, a[0].w, a[1].w, a[2].w, a[3].w};
+        const uint32_t vb[32] = {b[0].x, b[1].x, b[2].x, b[3].x, b[4].x, b[5].x, b[6].x, b[7].x,
+                                 b[0].y, b[1].y, b[2].y, b[3].y, b[4].y, b[5].y, b[6].y, b[7].y,
+                                 b[0].z, b[1].z, b[2].z, b[3].z, b[4].z, b[5].z, b[6].z, b[7].z,
+                                 b[0].w, b[1].w, b[2].w, b[3].w, b[4].w, b[5].w, b[6].w, b[7].w};
+        tmem_st16(sf, va);
+        tmem_st32(sf + 16, vb);
     } else {
-        uint32_t a[4], b[8];
+        uint32_t v[8], w[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) a[c] = *reinterpret_cast<const uint32_t*>(ua + (lane + 32 * c) * W);
+        for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint32_t*>(ua + (lane + 32 * c) * W);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) b[c] = *reinterpret_cast<const uint32_t*>(ub + (lane + 32 * c) * W);
-        tmem_st4(sf + 0, a[0], a[1], a[2], a[3]);
-        tmem_st4(sf + 4, b[0], b[1], b[2], b[3]);
-        tmem_st4(sf + 8, b[4], b[5], b[6], b[7]);
+        for (int c = 0; c < 4; ++c) v[4 + c] = *reinterpret_cast<const uint32_t*>(ub + (lane + 32 * c) * W);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint32_t*>(ub + (lane + 128 + 32 * c) * W);
+        // SFA in columns sf .. sf+3, SFB in sf+4 .. sf+11 (byte j = MMA j): an x8 and an x4 store
+        tmem_st8(sf, v);
+        tmem_st4(sf + 8, w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -1010,19 +1041,26 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         // ------------------------------------------------ warps 0-3: scale writers
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
         const uint32_t ready0 = leader_addr(&sf_ready[0]);
-        for (int gk = 0; gk < total_kb; ++gk) {
-            const int u = gk / G, r = u % R, t = gk % T;
+        // Two K-blocks per pass (G is even, so both come from one staged unit): both slots'
+        // stores are covered by one tcgen05.wait::st, which is most of a pass's latency.
+        static_assert(G % 2 == 0, "writer passes take K-blocks in pairs");
+        for (int gk = 0; gk < total_kb; gk += 2) {
+            const int u = gk / G, r = u % R, t0 = gk % T, t1 = (gk + 1) % T;
             if (!mbar_wait(&sf_full[r], (uint32_t)(u / R) & 1u)) break;
-            if (!mbar_wait_pair(T == S ? &empty[t] : &sf_free[t], ((uint32_t)(gk / T) & 1u) ^ 1u)) break;
+            if (!mbar_wait_pair(T == S ? &empty[t0] : &sf_free[t0], ((uint32_t)(gk / T) & 1u) ^ 1u)) break;
+            if (!mbar_wait_pair(T == S ? &empty[t1] : &sf_free[t1], ((uint32_t)((gk + 1) / T) & 1u) ^ 1u)) break;
             tc_fence_after();
-            const uint32_t sf = tmem + lane_base + kSfCol + (uint32_t)t * kSfCols;
-            write_unit_scales<kKind>(sf_stage + r * kSfUnit, gk % G, p.b_sc_2d != 0, sf, lane);
+            write_unit_scales<kKind>(sf_stage + r * kSfUnit, gk % G, p.b_sc_2d != 0,
+                                     tmem + lane_base + kSfCol + (uint32_t)t0 * kSfCols, lane);
+            write_unit_scales<kKind>(sf_stage + r * kSfUnit, (gk + 1) % G, p.b_sc_2d != 0,
+                                     tmem + lane_base + kSfCol + (uint32_t)t1 * kSfCols, lane);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive_cluster(ready0 + (uint32_t)t * 8u);
-                if (gk % G == G - 1) mbar_arrive(&sf_empty[r]);
+                mbar_arrive_cluster(ready0 + (uint32_t)t0 * 8u);
+                mbar_arrive_cluster(ready0 + (uint32_t)t1 * 8u);
+                if ((gk + 1) % G == G - 1) mbar_arrive(&sf_empty[r]);
             }
         }
     } else {
@@ -1114,9 +1152,9 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2D uint8 tensor map: [rows][row_bytes], box {128 B, box_rows}, 128-byte swizzle.
-// 2D uint8 tensor map over scale rows: [rows][row_bytes], box {box_w B, box_rows}, no swizzle.
+// 2D uint8 tensor map over scale rows: [rows][row_bytes], box {box_w B, box_rows}.
 bool make_map_sf(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_w,
-                 uint32_t box_rows) {
+                 uint32_t box_rows, CUtensorMapSwizzle swz) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {row_bytes, rows};
@@ -1124,7 +1162,7 @@ bool make_map_sf(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t 
     cuuint32_t box[2] = {box_w, box_rows};
     cuuint32_t es[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1213,10 +1251,12 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
     if (!make_map(&p.tma_b, a.b, kbytes, (uint64_t)a.N, 128)) return cudaErrorInvalidValue;
     const uint64_t sc_ld = kKind == 0 ? (uint64_t)a.K / 16 : (uint64_t)a.K / 32;
     const bool b2d = kKind == 0 && a.b_scale_kind == 2;
-    if (!make_map_sf(&p.tma_sfa, a.a_scales, sc_ld, (uint64_t)a.M, sf_unit_w<kKind>(), kBM))
+    // NVFP4 scale rows (64 bytes) land with the 64-byte swizzle the writers read them through
+    const CUtensorMapSwizzle sf_swz = kKind == 0 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (!make_map_sf(&p.tma_sfa, a.a_scales, sc_ld, (uint64_t)a.M, sf_unit_w<kKind>(), kBM, sf_swz))
         return cudaErrorInvalidValue;
     if (!make_map_sf(&p.tma_sfb, a.b_scales, sc_ld, b2d ? (uint64_t)a.N / 16 : (uint64_t)a.N, sf_unit_w<kKind>(),
-                     b2d ? 16 : kBN))
+                     b2d ? 16 : kBN, sf_swz))
         return cudaErrorInvalidValue;
     p.a_sc = a.a_scales;
     p.b_sc = a.b_scales;
