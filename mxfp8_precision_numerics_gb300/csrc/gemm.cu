@@ -171,18 +171,14 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b,
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
                  ::"r"(taddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
-// tcgen05.st of 8 / 16 / 32 consecutive columns (one 32-bit register per column and lane)
+// tcgen05.st of 1 / 8 / 32 consecutive columns (one 32-bit register per column and lane)
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
                  ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
                    "r"(v[7]) : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11,"
-                 " %12, %13, %14, %15, %16};"
-                 ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
-                   "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-                   "r"(v[15]) : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11,"
@@ -765,52 +761,49 @@ constexpr uint32_t kIdesc2Mxfp8 = (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3)
                                   (1u << 23) | ((uint32_t)(256 >> 4) << 24);
 
 // Scale writer step of the pair kernel: K-block `sub` of a staged unit (rows W bytes apart)
-// into tensor memory, in the layout the tensor core reads (row r: lane r mod 32 of every lane
-// quarter, column base + r/32). b2d: B holds one scale row per 16 rows (16 x 16 tiles).
+// into tensor memory, in the layout the tensor core reads: scale row r at lane r mod 32,
+// column base + r/32. The tensor core's lane quarter q computes A rows 32q .. 32q+31 and reads
+// their scales from its own lanes only (column base + q), so warp q writes just that column of
+// the A scales; every quarter multiplies all 256 B rows, so each gets all B-scale columns.
+// b2d: B holds one scale row per 16 rows (16 x 16 tiles).
 template <int kKind>
-__device__ __forceinline__ void write_unit_scales(const uint8_t* unit, int sub, bool b2d, uint32_t sf, int lane) {
+__device__ __forceinline__ void write_unit_scales(const uint8_t* unit, int sub, bool b2d, uint32_t sf, int lane,
+                                                  int quarter) {
     constexpr uint32_t W = sf_unit_w<kKind>();
-    const uint8_t* ua = unit + sub * Cfg<kKind>::kSfRowBytes;
-    const uint8_t* ub = unit + sf_unit_a<kKind>() + sub * Cfg<kKind>::kSfRowBytes;
+    const uint8_t* a0 = unit;
+    const uint8_t* b0 = unit + sf_unit_a<kKind>();
     static_assert(kKind != 0 || W == 64, "the NVFP4 swizzle below assumes 64-byte scale rows");
+    const int ra = lane + 32 * quarter;
     if (kKind == 0) {
         // NVFP4 units arrive with the TMA's 64-byte swizzle: the 16-byte chunk `sub` of row r
         // sits at chunk sub ^ ((r >> 1) & 3), so the 8 lanes of a quarter-warp read 8 distinct
-        // bank groups (with plain 64-byte rows they collided 4 ways)
-        const uint8_t* a0 = unit;
-        const uint8_t* b0 = unit + sf_unit_a<kKind>();
-        uint4 a[4], b[8];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int r = lane + 32 * c;
-            a[c] = *reinterpret_cast<const uint4*>(a0 + r * W + 16 * (sub ^ ((r >> 1) & 3)));
-        }
+        // bank groups
+        const uint4 a = *reinterpret_cast<const uint4*>(a0 + ra * W + 16 * (sub ^ ((ra >> 1) & 3)));
+        uint4 b[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             const int r = b2d ? ((lane + 32 * c) >> 4) : lane + 32 * c;
             b[c] = *reinterpret_cast<const uint4*>(b0 + r * W + 16 * (sub ^ ((r >> 1) & 3)));
         }
-        // MMA j: SFA in columns sf + 4j + c (c = row / 32), SFB in columns sf + 16 + 8j + c;
-        // the 16 SFA and 32 SFB columns are consecutive: one x16 and one x32 store
-        const uint32_t va[16] = {a[0].x, a[1].x, a[2].x, a[3].x, a[0].y, a[1].y, a[2].y, a[3].y,
-                                 a[0].z, a[1].z, a[2].z, a[3].z, a[0].w, a[1].w, a[2].w, a[3].w};
+        // MMA j: SFA in column sf + 4j + quarter; SFB in columns sf + 16 + 8j + c (c = row / 32),
+        // 32 consecutive columns: one x32 store
+        tmem_st1(sf + 0 + quarter, a.x);
+        tmem_st1(sf + 4 + quarter, a.y);
+        tmem_st1(sf + 8 + quarter, a.z);
+        tmem_st1(sf + 12 + quarter, a.w);
         const uint32_t vb[32] = {b[0].x, b[1].x, b[2].x, b[3].x, b[4].x, b[5].x, b[6].x, b[7].x,
                                  b[0].y, b[1].y, b[2].y, b[3].y, b[4].y, b[5].y, b[6].y, b[7].y,
                                  b[0].z, b[1].z, b[2].z, b[3].z, b[4].z, b[5].z, b[6].z, b[7].z,
                                  b[0].w, b[1].w, b[2].w, b[3].w, b[4].w, b[5].w, b[6].w, b[7].w};
-        tmem_st16(sf, va);
         tmem_st32(sf + 16, vb);
     } else {
-        uint32_t v[8], w[4];
+        const uint32_t a = *reinterpret_cast<const uint32_t*>(a0 + ra * W + 4 * sub);
+        uint32_t b[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint32_t*>(ua + (lane + 32 * c) * W);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) v[4 + c] = *reinterpret_cast<const uint32_t*>(ub + (lane + 32 * c) * W);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint32_t*>(ub + (lane + 128 + 32 * c) * W);
-        // SFA in columns sf .. sf+3, SFB in sf+4 .. sf+11 (byte j = MMA j): an x8 and an x4 store
-        tmem_st8(sf, v);
-        tmem_st4(sf + 8, w[0], w[1], w[2], w[3]);
+        for (int c = 0; c < 8; ++c) b[c] = *reinterpret_cast<const uint32_t*>(b0 + (lane + 32 * c) * W + 4 * sub);
+        // SFA in column sf + quarter, SFB in sf + 4 .. sf + 11 (byte j = MMA j)
+        tmem_st1(sf + quarter, a);
+        tmem_st8(sf + 4, b);
     }
 }
 
@@ -1051,9 +1044,9 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
             if (!mbar_wait_pair(T == S ? &empty[t1] : &sf_free[t1], ((uint32_t)((gk + 1) / T) & 1u) ^ 1u)) break;
             tc_fence_after();
             write_unit_scales<kKind>(sf_stage + r * kSfUnit, gk % G, p.b_sc_2d != 0,
-                                     tmem + lane_base + kSfCol + (uint32_t)t0 * kSfCols, lane);
+                                     tmem + lane_base + kSfCol + (uint32_t)t0 * kSfCols, lane, warp);
             write_unit_scales<kKind>(sf_stage + r * kSfUnit, (gk + 1) % G, p.b_sc_2d != 0,
-                                     tmem + lane_base + kSfCol + (uint32_t)t1 * kSfCols, lane);
+                                     tmem + lane_base + kSfCol + (uint32_t)t1 * kSfCols, lane, warp);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
