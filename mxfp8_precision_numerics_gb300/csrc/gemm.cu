@@ -1096,23 +1096,24 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) epi_bf16(p, pk[c], row, row_ok, col0 + 32 * c, amax_bits);
             } else {
-                // fp32 output: loads interleaved with the stores of the previous chunk
-                uint32_t ra[32], rb[32];
+                // fp32 output: two chunks in flight; the first two are stored while the last two
+                // load, then tensor memory goes back to the MMAs (at most 96 live registers)
+                uint32_t ra[32], rb[32], rc[32];
                 tmem_ld32_async(tacc, ra);
-                tmem_wait_ld(ra);
                 tmem_ld32_async(tacc + 32, rb);
+                tmem_wait_ld(ra);
+                tmem_ld32_async(tacc + 64, rc);
                 store_chunk(p, ra, row, row_ok, col0, alpha);
                 tmem_wait_ld(rb);
-                tmem_ld32_async(tacc + 64, ra);
+                tmem_ld32_async(tacc + 96, ra);
                 store_chunk(p, rb, row, row_ok, col0 + 32, alpha);
+                tmem_wait_ld(rc);
                 tmem_wait_ld(ra);
-                tmem_ld32_async(tacc + 96, rb);
-                store_chunk(p, ra, row, row_ok, col0 + 64, alpha);
-                tmem_wait_ld(rb);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_leader);
-                store_chunk(p, rb, row, row_ok, col0 + 96, alpha);
+                store_chunk(p, rc, row, row_ok, col0 + 64, alpha);
+                store_chunk(p, ra, row, row_ok, col0 + 96, alpha);
             }
         }
         epi_flush_amax(p, amax_bits, lane);
