@@ -311,6 +311,86 @@ EXPORT void orc_quantize_1d(const uint16_t* x, int64_t rows, int64_t cols, int64
 }
 
 /* ------------------------------------------------------------------------- */
+/* NVFP4 1D quantize with a per-row (per-token) FP32 outer scale and, when     */
+/* four_six is set, the Four Over Six choice of block scale.                   */
+/* [VZ] §10: 4/6 tries a second scale per block that puts the block maximum   */
+/* on 4 instead of 6 and keeps the version with the smaller error (the choice  */
+/* lives in the block scale; activations only), and the activation outer      */
+/* scale is computed separately for each token's row (QLinearFn listing:      */
+/* outer="row", four_six=True for x; outer="tensor" for w). [TML] "方案细节":   */
+/* 4/6 on activations, not weights; per-token outer scale for activations.    */
+/* Readings where the pages are silent:                                       */
+/*   - a row's s_enc / s_dec are orc_global_scales of that row's own amax;    */
+/*   - candidate c (target c = 6 or c = 4) is the per-tensor block rule with  */
+/*     6 replaced by c: sb_c = e4m3_rne_sat((amax_b / c) * s_enc), raised to  */
+/*     0x01 if 0; s_enc_b = 1 / (fp32(sb_c) * s_dec); y_i = x_i * s_enc_b;    */
+/*     code_i = e2m1_rne(y_i). Where (amax_b / 4) * s_enc exceeds 448 the      */
+/*     scale saturates and the maximum lands between 4 and 6;                 */
+/*   - "error" is the block's squared error. With S_c = fp32(sb_c) and q_i    */
+/*     the E2M1 value of code_i, x_i - x^_i = s_dec * S_c * (y_i - q_i) up to */
+/*     the rounding of y_i, and s_dec is the same for both candidates, so the */
+/*     compared quantity is E_c = (sum_i (y_i - q_i)^2) * S_c^2 in fp32. Each */
+/*     y_i - q_i is exact (q_i is the grid point nearest y_i, |y_i| < 12);    */
+/*     the squares go into two sums, one over the even positions and one over */
+/*     the odd, each built in index order with fused multiply-adds (one       */
+/*     rounding per step); E_c = (even + odd) * S_c^2 (S_c^2 is exact);       */
+/*   - the 4 candidate is kept only if E_4 < E_6 (a tie keeps 6).             */
+/* ------------------------------------------------------------------------- */
+
+/* One candidate for the 16 bf16 values xb (amax_b = max |xb|): its scale code,
+ * its 16 codes and its error E_c. */
+EXPORT void orc_nvfp4_block_candidate(const uint16_t* xb, float target, float s_enc, float s_dec,
+                                      uint32_t* sb_out, uint8_t* codes16, float* err_out)
+{
+    float amax_b = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+        float a = fabsf(bf16_value(xb[i]));
+        if (a > amax_b) amax_b = a;
+    }
+    uint32_t sb = orc_e4m3_encode_rne_sat((amax_b / target) * s_enc) & 0x7Fu;
+    if (sb == 0) sb = 1;
+    float s_enc_b = orc_block_encode_scale(sb, s_dec);
+    float even = 0.0f, odd = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+        float y = bf16_value(xb[i]) * s_enc_b;
+        uint32_t code = orc_e2m1_encode_rne(y);
+        float d = y - (float)orc_e2m1_decode(code);
+        if (i & 1) odd = fmaf(d, d, odd);
+        else       even = fmaf(d, d, even);
+        codes16[i] = (uint8_t)code;
+    }
+    float S = (float)orc_e4m3_decode(sb);
+    *sb_out = sb;
+    *err_out = (even + odd) * (S * S);
+}
+
+/* codes [rows][cols/2], scales [rows][cols/16], s_dec_rows [rows]. */
+EXPORT void orc_quantize_1d_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                                 int four_six, uint8_t* codes, uint8_t* scales, float* s_dec_rows)
+{
+    int64_t nb = cols / 16;
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t* xr = x + r * ld;
+        float s_enc, s_dec;
+        orc_global_scales(orc_amax_bf16(xr, 1, cols, cols), &s_enc, &s_dec);
+        for (int64_t b = 0; b < nb; ++b) {
+            uint32_t sb, sb4;
+            uint8_t c6[16], c4[16];
+            float e6, e4;
+            orc_nvfp4_block_candidate(xr + b * 16, 6.0f, s_enc, s_dec, &sb, c6, &e6);
+            const uint8_t* c = c6;
+            if (four_six) {
+                orc_nvfp4_block_candidate(xr + b * 16, 4.0f, s_enc, s_dec, &sb4, c4, &e4);
+                if (e4 < e6) { sb = sb4; c = c4; }
+            }
+            scales[r * nb + b] = (uint8_t)sb;
+            for (int i = 0; i < 16; ++i) put_code(codes, cols / 2, r, b * 16 + i, c[i]);
+        }
+        s_dec_rows[r] = s_dec;
+    }
+}
+
+/* ------------------------------------------------------------------------- */
 /* NVFP4 2D quantize: one scale per 16x16 tile ([NV] "Two-Dimensional Weight   */
 /* Scaling"; [VZ] §8). tile_scales: [rows/16][cols/16].                        */
 /* ------------------------------------------------------------------------- */
@@ -354,7 +434,7 @@ static double nvfp4_value(const uint8_t* codes, const uint8_t* scales, int scale
 {
     (void)rows;
     uint32_t sb = (scale_kind == 2) ? scales[(r / 16) * (cols / 16) + c / 16]
-                                    : scales[r * (cols / 16) + c / 16];
+                                    : scales[r * (cols / 16) + c / 16];   /* kinds 1 and 3 */
     return orc_e2m1_decode(get_code(codes, cols / 2, r, c)) * orc_e4m3_decode(sb) * s_dec;
 }
 
@@ -365,6 +445,19 @@ EXPORT void orc_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales, int s
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t c = 0; c < cols; ++c) {
             double v = nvfp4_value(codes, scales, scale_kind, (double)s_dec, rows, cols, r, c);
+            if (out_f32) out_f32[r * cols + c] = (float)v;
+            if (out_f64) out_f64[r * cols + c] = v;
+        }
+}
+
+/* NVFP4 with 1D scales and a per-row outer scale (orc_quantize_1d_rows):
+ * value = code x block scale x s_dec_rows[r]. */
+EXPORT void orc_dequant_nvfp4_rows(const uint8_t* codes, const uint8_t* scales, const float* s_dec_rows,
+                                   int64_t rows, int64_t cols, float* out_f32, double* out_f64)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            double v = nvfp4_value(codes, scales, 1, (double)s_dec_rows[r], rows, cols, r, c);
             if (out_f32) out_f32[r * cols + c] = (float)v;
             if (out_f64) out_f64[r * cols + c] = v;
         }
@@ -440,13 +533,14 @@ EXPORT void orc_mxfp8_block(const float* v, int rounding, uint64_t seed, uint32_
 /* [VZ] §9-10 (dequantize, transpose, re-quantize to MXFP8 with SR);           */
 /* [TML] "基于随机舍入的重量化"; [NV] "Random Hadamard Transforms" (wgrad only). */
 /* in_kind: 0 = bf16 [rows][cols]; 1 = NVFP4 with 1D scales; 2 = NVFP4 with    */
-/*          16x16 tile scales.                                                 */
+/*          16x16 tile scales; 3 = NVFP4 with 1D scales and a per-row outer     */
+/*          scale s_dec_rows[rows] (s_dec unused).                             */
 /* Output: transpose ? [cols][rows] : [rows][cols], E8M0 per 32 along the       */
 /*         output's contiguous dimension.                                      */
 /* ------------------------------------------------------------------------- */
 /* Output rows [orow_begin, orow_end) only; out_e4m3 / out_e8m0 hold just those rows. */
 EXPORT void orc_requant_mxfp8_rows(int in_kind, const void* in, const uint8_t* in_scales, float s_dec,
-                                   int64_t rows, int64_t cols, int transpose, int rht, uint32_t rht_signs,
+                                   const float* s_dec_rows, int64_t rows, int64_t cols, int transpose, int rht, uint32_t rht_signs,
                                    int rounding, uint64_t seed, uint32_t tag,
                                    int64_t orow_begin, int64_t orow_end,
                                    uint8_t* out_e4m3, uint8_t* out_e8m0)
@@ -460,7 +554,8 @@ EXPORT void orc_requant_mxfp8_rows(int in_kind, const void* in, const uint8_t* i
                 int64_t r = transpose ? oc : orow;     /* source coordinates */
                 int64_t c = transpose ? orow : oc;
                 if (in_kind == 0) v[i] = bf16_value(((const uint16_t*)in)[r * cols + c]);
-                else v[i] = (float)nvfp4_value((const uint8_t*)in, in_scales, in_kind, (double)s_dec,
+                else v[i] = (float)nvfp4_value((const uint8_t*)in, in_scales, in_kind,
+                                               in_kind == 3 ? (double)s_dec_rows[r] : (double)s_dec,
                                                rows, cols, r, c);
             }
             if (rht) { orc_rht16_group(v, rht_signs); orc_rht16_group(v + 16, rht_signs); }
@@ -472,10 +567,10 @@ EXPORT void orc_requant_mxfp8_rows(int in_kind, const void* in, const uint8_t* i
 }
 
 EXPORT void orc_requant_mxfp8(int in_kind, const void* in, const uint8_t* in_scales, float s_dec,
-                              int64_t rows, int64_t cols, int transpose, int rht, uint32_t rht_signs,
+                              const float* s_dec_rows, int64_t rows, int64_t cols, int transpose, int rht, uint32_t rht_signs,
                               int rounding, uint64_t seed, uint32_t tag,
                               uint8_t* out_e4m3, uint8_t* out_e8m0)
 {
-    orc_requant_mxfp8_rows(in_kind, in, in_scales, s_dec, rows, cols, transpose, rht, rht_signs,
+    orc_requant_mxfp8_rows(in_kind, in, in_scales, s_dec, s_dec_rows, rows, cols, transpose, rht, rht_signs,
                            rounding, seed, tag, 0, transpose ? cols : rows, out_e4m3, out_e8m0);
 }

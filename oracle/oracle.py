@@ -29,7 +29,7 @@ _f64p = ctypes.POINTER(ctypes.c_double)
 _i64 = ctypes.c_int64
 
 RNE, SR = 0, 1
-IN_BF16, IN_NVFP4_1D, IN_NVFP4_2D = 0, 1, 2
+IN_BF16, IN_NVFP4_1D, IN_NVFP4_2D, IN_NVFP4_1D_ROWS = 0, 1, 2, 3
 
 
 def lib():
@@ -66,6 +66,13 @@ def lib():
         for fn in (L.orc_quantize_1d, L.orc_quantize_2d):
             fn.restype = None
             fn.argtypes = [_u16p, _i64, _i64, _i64, _f32p, _u8p, _u8p, _f32p, _f32p]
+        L.orc_nvfp4_block_candidate.restype = None
+        L.orc_nvfp4_block_candidate.argtypes = [_u16p, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                                _u32p, _u8p, _f32p]
+        L.orc_quantize_1d_rows.restype = None
+        L.orc_quantize_1d_rows.argtypes = [_u16p, _i64, _i64, _i64, ctypes.c_int, _u8p, _u8p, _f32p]
+        L.orc_dequant_nvfp4_rows.restype = None
+        L.orc_dequant_nvfp4_rows.argtypes = [_u8p, _u8p, _f32p, _i64, _i64, _f32p, _f64p]
         L.orc_dequant_nvfp4.restype = None
         L.orc_dequant_nvfp4.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_float, _i64, _i64,
                                         _f32p, _f64p]
@@ -80,12 +87,12 @@ def lib():
                                       ctypes.c_uint64, _u8p, _u8p]
         L.orc_requant_mxfp8_rows.restype = None
         L.orc_requant_mxfp8_rows.argtypes = [ctypes.c_int, ctypes.c_void_p, _u8p, ctypes.c_float,
-                                             _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
+                                             _f32p, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
                                              ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32, _i64, _i64,
                                              _u8p, _u8p]
         L.orc_requant_mxfp8.restype = None
         L.orc_requant_mxfp8.argtypes = [ctypes.c_int, ctypes.c_void_p, _u8p, ctypes.c_float,
-                                        _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
+                                        _f32p, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
                                         ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32, _u8p, _u8p]
         _LIB = L
     return _LIB
@@ -184,6 +191,45 @@ def quantize_2d(w, amax=None):
     return _quantize(lib().orc_quantize_2d, w, amax, tile=True)
 
 
+def nvfp4_block_candidate(xb, target, s_enc, s_dec):
+    """One 4/6 candidate for 16 bf16 values (uint16 bits), target 6.0 or 4.0
+    -> (scale code, codes[16], error E_c)."""
+    xb = _c(xb, np.uint16)
+    assert xb.size == 16
+    sb = ctypes.c_uint32()
+    codes = np.zeros(16, np.uint8)
+    err = ctypes.c_float()
+    lib().orc_nvfp4_block_candidate(_p(xb, _u16p), float(target), float(s_enc), float(s_dec),
+                                    ctypes.byref(sb), _p(codes, _u8p), ctypes.byref(err))
+    return sb.value, codes, err.value
+
+
+def quantize_1d_rows(x, four_six=True):
+    """NVFP4 1x16 blocks with a per-row outer scale (and 4/6 if four_six)
+    -> (codes, scales, s_dec_rows float32[rows])."""
+    x = _c(x, np.uint16)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    scales = np.zeros((rows, cols // 16), np.uint8)
+    s_dec = np.zeros(rows, np.float32)
+    lib().orc_quantize_1d_rows(_p(x, _u16p), rows, cols, cols, int(bool(four_six)),
+                               _p(codes, _u8p), _p(scales, _u8p), _p(s_dec, _f32p))
+    return codes, scales, s_dec
+
+
+def dequant_nvfp4_rows(codes, scales, s_dec_rows, as_f32=False):
+    """1D scales with a per-row outer scale s_dec_rows[rows]."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    sd = _c(s_dec_rows, np.float32)
+    rows, cols = codes.shape[0], codes.shape[1] * 2
+    out = np.zeros((rows, cols), np.float32 if as_f32 else np.float64)
+    lib().orc_dequant_nvfp4_rows(_p(codes, _u8p), _p(scales, _u8p), _p(sd, _f32p), rows, cols,
+                                 _p(out, _f32p) if as_f32 else None,
+                                 None if as_f32 else _p(out, _f64p))
+    return out
+
+
 def dequant_nvfp4(codes, scales, scale_kind, s_dec, as_f32=False):
     """scale_kind 1 = 1D [rows, cols/16], 2 = tiles [rows/16, cols/16]."""
     codes = _c(codes, np.uint8)
@@ -235,7 +281,13 @@ def mxfp8_block(v, rounding=RNE, seed=0, tag=0, out_idx0=0):
 def requant_mxfp8(in_kind, data, scales, s_dec, rows, cols, transpose, rht, rht_signs,
                   rounding, seed, tag, out_rows=None):
     """Dequantize -> [transpose] -> [RHT16] -> MXFP8 -> (e4m3, e8m0).
+    in_kind IN_NVFP4_1D_ROWS takes s_dec as an array of per-row outer scales.
     out_rows=(begin, end) computes only those output rows."""
+    sd_rows = None
+    if in_kind == IN_NVFP4_1D_ROWS:
+        sd_rows = _c(s_dec, np.float32)
+        assert sd_rows.shape == (rows,)
+        s_dec = 0.0
     if in_kind == IN_BF16:
         data = _c(data, np.uint16)
         sc = None
@@ -247,7 +299,8 @@ def requant_mxfp8(in_kind, data, scales, s_dec, rows, cols, transpose, rht, rht_
     b, e = (0, orows) if out_rows is None else out_rows
     e4 = np.zeros((e - b, ocols), np.uint8)
     e8 = np.zeros((e - b, ocols // 32), np.uint8)
-    lib().orc_requant_mxfp8_rows(in_kind, data.ctypes.data, sc, float(s_dec), rows, cols,
+    lib().orc_requant_mxfp8_rows(in_kind, data.ctypes.data, sc, float(s_dec),
+                                 None if sd_rows is None else _p(sd_rows, _f32p), rows, cols,
                                  int(bool(transpose)), int(bool(rht)), int(rht_signs), rounding,
                                  int(seed), int(tag), b, e, _p(e4, _u8p), _p(e8, _u8p))
     return e4, e8
@@ -257,6 +310,13 @@ def requant_mxfp8(in_kind, data, scales, s_dec, rows, cols, transpose, rht, rht_
 def gemm_nvfp4(a_codes, a_scales, a_kind, a_sdec, b_codes, b_scales, b_kind, b_sdec):
     """D = A . B^T on exactly dequantized NVFP4 operands, float64."""
     A = dequant_nvfp4(a_codes, a_scales, a_kind, a_sdec)
+    B = dequant_nvfp4(b_codes, b_scales, b_kind, b_sdec)
+    return A @ B.T
+
+
+def gemm_nvfp4_rows(a_codes, a_scales, a_sdec_rows, b_codes, b_scales, b_kind, b_sdec):
+    """D = A . B^T with A carrying a per-row outer scale, float64."""
+    A = dequant_nvfp4_rows(a_codes, a_scales, a_sdec_rows)
     B = dequant_nvfp4(b_codes, b_scales, b_kind, b_sdec)
     return A @ B.T
 
