@@ -59,7 +59,8 @@ enum fp4q_status {
     FP4Q_ERR_UNSUPPORTED = 7  /* the current device is not sm_103 / sm_100 class          */
 };
 
-enum fp4q_in_kind { FP4Q_IN_BF16 = 0, FP4Q_IN_NVFP4_1D = 1, FP4Q_IN_NVFP4_2D = 2 };
+enum fp4q_in_kind { FP4Q_IN_BF16 = 0, FP4Q_IN_NVFP4_1D = 1, FP4Q_IN_NVFP4_2D = 2,
+                    FP4Q_IN_NVFP4_1D_ROWS = 3 };
 enum fp4q_rounding { FP4Q_RNE = 0, FP4Q_SR = 1 };
 enum fp4q_dtype { FP4Q_F32 = 0, FP4Q_BF16 = 1 };
 enum fp4q_scale_kind { FP4Q_SCALE_1D = 1, FP4Q_SCALE_2D = 2 };
@@ -90,6 +91,33 @@ FP4Q_API int fp4q_version(void);
 FP4Q_API int fp4q_quantize_1d(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld,
                      const float* amax_in, float* amax_ws,
                      uint8_t* codes, uint8_t* scales, float* s_dec_out, fp4q_stream_t stream);
+
+/*
+ * fp4q_quantize_1d_rows — NVFP4 quantize with 1x16 blocks along each row, one FP32 outer scale
+ * per row (per token) and, if four_six, the Four Over Six block-scale choice: the activation
+ * quantizer of 4bit.vizuara.ai §10 (QLinearFn: outer="row", four_six=True) and of the
+ * Thinking Machines recipe ("End-to-End 4-Bit Training", 方案细节). One pass over x; no
+ * amax kernel and no workspace.
+ *   per row r: amax_r = max |x[r, :]|; s_enc = 2688 / amax_r, s_dec = 1 / s_enc (fp32;
+ *              amax_r == 0 -> 1 and 1); s_dec_rows[r] = s_dec
+ *   per block, candidate c = 6 (and c = 4 when four_six):
+ *              sb_c = E4M3_RNE((amax_b / c) * s_enc), saturating, raised to 0x01 if 0;
+ *              s_enc_b = 1 / (fp32(sb_c) * s_dec); y_i = x_i * s_enc_b; code_i = E2M1_RNE(y_i)
+ *              E_c = (sum_i (y_i - q_i)^2) * fp32(sb_c)^2, q_i = E2M1 value of code_i; the
+ *              squares are summed with fused multiply-adds in two chains (even positions,
+ *              odd positions), each in index order, and the chains are added
+ *              the block keeps candidate 4 iff E_4 < E_6 (the choice lives in the scale byte)
+ *   x_bf16      [rows][ld] bf16, 16-byte aligned, ld % 8 == 0, ld >= cols
+ *   four_six    0 or 1
+ *   codes       [rows][cols/2] bytes, 16-byte aligned; scales [rows][cols/16] E4M3 bytes
+ *   s_dec_rows  device float[rows]
+ *   rows >= 1, cols >= 16, cols % 16 == 0.
+ * Decode: x^[r, k] = E2M1(code) * E4M3(scale) * s_dec_rows[r]; fp4q_gemm_nvfp4_rows and the
+ * requantize input kind FP4Q_IN_NVFP4_1D_ROWS take this form.
+ */
+FP4Q_API int fp4q_quantize_1d_rows(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld,
+                     int four_six, uint8_t* codes, uint8_t* scales, float* s_dec_rows,
+                     fp4q_stream_t stream);
 
 /*
  * fp4q_quantize_2d — NVFP4 quantize of a weight with one E4M3 scale per 16x16 tile, so the
@@ -143,7 +171,10 @@ FP4Q_API int fp4q_quantize_2d_noalloc(const void* w_bf16, int64_t rows, int64_t 
  *             FP4Q_IN_NVFP4_1D: in = codes [rows][cols/2], in_scales [rows][cols/16],
  *                               in_s_dec = device float
  *             FP4Q_IN_NVFP4_2D: in = codes [rows][cols/2], in_scales [rows/16][cols/16]
- *   dequantized value (fp32) = (E2M1(code) * E4M3(scale)) * s_dec
+ *             FP4Q_IN_NVFP4_1D_ROWS: as FP4Q_IN_NVFP4_1D with in_s_dec = device float[rows],
+ *                               one outer scale per input row (fp4q_quantize_1d_rows)
+ *   dequantized value (fp32) = (E2M1(code) * E4M3(scale)) * s_dec (of the input row for
+ *             FP4Q_IN_NVFP4_1D_ROWS)
  *   transpose 0: output [rows][cols]; 1: output [cols][rows]. MXFP8 blocks of 32 and the
  *             Hadamard groups of 16 run along the OUTPUT's contiguous dimension.
  *   rht       0 / 1. The transform on each group of 16: y = (1/4) H16 (s o x), Sylvester H16,
@@ -201,6 +232,18 @@ FP4Q_API int fp4q_gemm_nvfp4(const uint8_t* a, const uint8_t* a_scales, const fl
                     int groups, const int64_t* group_row_offsets_host, fp4q_stream_t stream);
 
 /*
+ * fp4q_gemm_nvfp4_rows — fp4q_gemm_nvfp4 with one outer scale per row of A, the activation form
+ * of 4bit.vizuara.ai §10 (per-token outer scale; fp4q_quantize_1d_rows produces it):
+ *   D[m,n] = s_dec_a[m] * s_dec_b[g] * sum_blocks sa[m,blk] * sb[n,blk] * sum_{k in blk} a_k b_k
+ *   a_s_dec_rows  device float[M]; every other argument as fp4q_gemm_nvfp4.
+ */
+FP4Q_API int fp4q_gemm_nvfp4_rows(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec_rows,
+                    const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
+                    const float* b_s_dec, void* d, int d_dtype,
+                    int64_t M, int64_t N, int64_t K,
+                    int groups, const int64_t* group_row_offsets_host, fp4q_stream_t stream);
+
+/*
  * fp4q_gemm_mxfp8 — block-scaled MXFP8 x MXFP8 GEMM, D = A . B^T, FP32 accumulation on the
  * tcgen05 tensor cores (the dgrad and wgrad GEMMs of the backward pass). [VZ] §8 and §10:
  * dx = g . w_q sums over N, dw = g^T . x_q sums over tokens; both operands carry their
@@ -229,6 +272,16 @@ FP4Q_API int fp4q_gemm_mxfp8(const uint8_t* a, const uint8_t* a_scales,
  *   act_out 16-byte aligned.
  */
 FP4Q_API int fp4q_gemm_nvfp4_gelu(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec,
+                    const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
+                    const float* b_s_dec, void* h_out, void* act_out, float* act_amax,
+                    int64_t M, int64_t N, int64_t K, fp4q_stream_t stream);
+
+/*
+ * fp4q_gemm_nvfp4_gelu_rows — fp4q_gemm_nvfp4_gelu with one outer scale per row of A
+ * (a_s_dec_rows, device float[M]). act_amax may be NULL (a per-row quantizer of act_out needs
+ * no tensor amax); if given it receives max |act_out| as in fp4q_gemm_nvfp4_gelu.
+ */
+FP4Q_API int fp4q_gemm_nvfp4_gelu_rows(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec_rows,
                     const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
                     const float* b_s_dec, void* h_out, void* act_out, float* act_amax,
                     int64_t M, int64_t N, int64_t K, fp4q_stream_t stream);

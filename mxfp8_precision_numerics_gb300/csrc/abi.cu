@@ -87,6 +87,18 @@ int fp4q_quantize_1d(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld,
                                                 codes, scales, s_dec_out, st));
 }
 
+int fp4q_quantize_1d_rows(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld, int four_six,
+                          uint8_t* codes, uint8_t* scales, float* s_dec_rows, fp4q_stream_t stream) {
+    if (four_six != 0 && four_six != 1) return FP4Q_ERR_ARG;
+    if (!x_bf16 || !codes || !scales || !s_dec_rows) return FP4Q_ERR_NULL;
+    if (rows < 1 || cols < 16 || cols % 16 != 0 || ld < cols) return FP4Q_ERR_SHAPE;
+    if (!al16(x_bf16) || ld % 8 != 0 || !al16(codes)) return FP4Q_ERR_ALIGN;
+    if (int d = check_device()) return d;
+    return cuda_status(fp4q::launch_quantize_1d_rows(static_cast<const uint16_t*>(x_bf16), rows, cols, ld,
+                                                     four_six, codes, scales, s_dec_rows,
+                                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fp4q_quantize_2d(const void* w_bf16, int64_t rows, int64_t cols, int64_t ld,
                      int64_t batch, int64_t batch_stride,
                      const float* amax_in, float* amax_ws,
@@ -116,7 +128,7 @@ int fp4q_requant_t_mxfp8_sr(int in_kind, const void* in, const uint8_t* in_scale
                             int transpose, int rht, uint32_t rht_signs,
                             int rounding, uint64_t seed, uint32_t tensor_tag,
                             uint8_t* out_e4m3, uint8_t* out_e8m0, fp4q_stream_t stream) {
-    if (in_kind < FP4Q_IN_BF16 || in_kind > FP4Q_IN_NVFP4_2D) return FP4Q_ERR_ARG;
+    if (in_kind < FP4Q_IN_BF16 || in_kind > FP4Q_IN_NVFP4_1D_ROWS) return FP4Q_ERR_ARG;
     if ((transpose != 0 && transpose != 1) || (rht != 0 && rht != 1)) return FP4Q_ERR_ARG;
     if (rounding != FP4Q_RNE && rounding != FP4Q_SR) return FP4Q_ERR_ARG;
     if (rht_signs > 0xFFFFu) return FP4Q_ERR_ARG;
@@ -166,11 +178,12 @@ static int validate_groups(int groups, const int64_t* offs, int64_t M) {
     return FP4Q_OK;
 }
 
-int fp4q_gemm_nvfp4(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec,
-                    const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
-                    const float* b_s_dec, void* d, int d_dtype,
-                    int64_t M, int64_t N, int64_t K,
-                    int groups, const int64_t* group_row_offsets_host, fp4q_stream_t stream) {
+// a_rows: a_s_dec holds one outer scale per row of A (M floats) instead of one
+static int gemm_nvfp4_impl(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec, int a_rows,
+                           const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
+                           const float* b_s_dec, void* d, int d_dtype,
+                           int64_t M, int64_t N, int64_t K,
+                           int groups, const int64_t* group_row_offsets_host, fp4q_stream_t stream) {
     if (b_scale_kind != FP4Q_SCALE_1D && b_scale_kind != FP4Q_SCALE_2D) return FP4Q_ERR_ARG;
     if (d_dtype != FP4Q_F32 && d_dtype != FP4Q_BF16) return FP4Q_ERR_ARG;
     if (!a || !a_scales || !a_s_dec || !b || !b_scales || !b_s_dec || !d) return FP4Q_ERR_NULL;
@@ -195,7 +208,26 @@ int fp4q_gemm_nvfp4(const uint8_t* a, const uint8_t* a_scales, const float* a_s_
     g.K = K;
     g.groups = groups;
     g.group_offsets = group_row_offsets_host;
+    g.a_sdec_rows = a_rows;
     return cuda_status(fp4q::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp4q_gemm_nvfp4(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec,
+                    const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
+                    const float* b_s_dec, void* d, int d_dtype,
+                    int64_t M, int64_t N, int64_t K,
+                    int groups, const int64_t* group_row_offsets_host, fp4q_stream_t stream) {
+    return gemm_nvfp4_impl(a, a_scales, a_s_dec, 0, b, b_scales, b_scale_kind, b_s_dec, d, d_dtype,
+                           M, N, K, groups, group_row_offsets_host, stream);
+}
+
+int fp4q_gemm_nvfp4_rows(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec_rows,
+                         const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
+                         const float* b_s_dec, void* d, int d_dtype,
+                         int64_t M, int64_t N, int64_t K,
+                         int groups, const int64_t* group_row_offsets_host, fp4q_stream_t stream) {
+    return gemm_nvfp4_impl(a, a_scales, a_s_dec_rows, 1, b, b_scales, b_scale_kind, b_s_dec, d, d_dtype,
+                           M, N, K, groups, group_row_offsets_host, stream);
 }
 
 int fp4q_gemm_mxfp8(const uint8_t* a, const uint8_t* a_scales,
@@ -227,19 +259,21 @@ int fp4q_gemm_mxfp8(const uint8_t* a, const uint8_t* a_scales,
     return cuda_status(fp4q::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int fp4q_gemm_nvfp4_gelu(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec,
-                         const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
-                         const float* b_s_dec, void* h_out, void* act_out, float* act_amax,
-                         int64_t M, int64_t N, int64_t K, fp4q_stream_t stream) {
+// a_rows: per-row outer scales of A (act_amax may then be NULL)
+static int gemm_nvfp4_gelu_impl(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec, int a_rows,
+                                const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
+                                const float* b_s_dec, void* h_out, void* act_out, float* act_amax,
+                                int64_t M, int64_t N, int64_t K, fp4q_stream_t stream) {
     if (b_scale_kind != FP4Q_SCALE_1D && b_scale_kind != FP4Q_SCALE_2D) return FP4Q_ERR_ARG;
-    if (!a || !a_scales || !a_s_dec || !b || !b_scales || !b_s_dec || !h_out || !act_out || !act_amax)
+    if (!a || !a_scales || !a_s_dec || !b || !b_scales || !b_s_dec || !h_out || !act_out ||
+        (!act_amax && !a_rows))
         return FP4Q_ERR_NULL;
     if (M < 1 || N < 16 || N % 16 != 0 || K < 256 || K % 256 != 0) return FP4Q_ERR_SHAPE;
     if (M > 2147483647 || N > 2147483647) return FP4Q_ERR_SHAPE;
     if (b_scale_kind == FP4Q_SCALE_2D && N % 16 != 0) return FP4Q_ERR_SHAPE;
     if (!al16(a) || !al16(b) || !al16(a_scales) || !al16(b_scales) || !al16(h_out) || !al16(act_out))
         return FP4Q_ERR_ALIGN;
-    if (!al4(act_amax)) return FP4Q_ERR_ALIGN;
+    if (act_amax && !al4(act_amax)) return FP4Q_ERR_ALIGN;
     if (int d = check_device()) return d;
     fp4q::GemmArgs g;
     g.kind = 0;
@@ -260,7 +294,24 @@ int fp4q_gemm_nvfp4_gelu(const uint8_t* a, const uint8_t* a_scales, const float*
     g.epi = 1;
     g.d2 = act_out;
     g.amax_out = act_amax;
+    g.a_sdec_rows = a_rows;
     return cuda_status(fp4q::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp4q_gemm_nvfp4_gelu(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec,
+                         const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
+                         const float* b_s_dec, void* h_out, void* act_out, float* act_amax,
+                         int64_t M, int64_t N, int64_t K, fp4q_stream_t stream) {
+    return gemm_nvfp4_gelu_impl(a, a_scales, a_s_dec, 0, b, b_scales, b_scale_kind, b_s_dec, h_out, act_out,
+                                act_amax, M, N, K, stream);
+}
+
+int fp4q_gemm_nvfp4_gelu_rows(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec_rows,
+                              const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
+                              const float* b_s_dec, void* h_out, void* act_out, float* act_amax,
+                              int64_t M, int64_t N, int64_t K, fp4q_stream_t stream) {
+    return gemm_nvfp4_gelu_impl(a, a_scales, a_s_dec_rows, 1, b, b_scales, b_scale_kind, b_s_dec, h_out,
+                                act_out, act_amax, M, N, K, stream);
 }
 
 int fp4q_gemm_mxfp8_dgelu(const uint8_t* a, const uint8_t* a_scales,

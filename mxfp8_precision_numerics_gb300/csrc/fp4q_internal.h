@@ -13,16 +13,19 @@ cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t l
 cudaError_t launch_quantize_1d(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
                                const float* amax, uint8_t* codes, uint8_t* scales, float* s_dec,
                                cudaStream_t st);
+cudaError_t launch_quantize_1d_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int four_six,
+                                    uint8_t* codes, uint8_t* scales, float* s_dec_rows, cudaStream_t st);
+void rows_shape(int64_t cols, int& W, int& hold);   // warps per row, blocks per thread
 cudaError_t launch_quantize_2d(const uint16_t* w, int64_t rows, int64_t cols, int64_t ld,
                                int64_t batch, int64_t batch_stride, const float* amax,
                                uint8_t* codes, uint8_t* tile_scales, float* s_dec,
                                cudaStream_t st);
 
 struct RequantArgs {
-    int in_kind;                 // 0 bf16, 1 NVFP4 1D, 2 NVFP4 2D
+    int in_kind;                 // 0 bf16, 1 NVFP4 1D, 2 NVFP4 2D, 3 NVFP4 1D with per-row s_dec
     const void* in;
     const uint8_t* in_scales;
-    const float* in_s_dec;
+    const float* in_s_dec;       // one float, or [rows] for kind 3
     int64_t rows, cols;
     int transpose, rht;
     uint32_t rht_signs;
@@ -40,7 +43,7 @@ struct GemmArgs {
     int kind;                    // 0 NVFP4, 1 MXFP8
     const uint8_t* a;
     const uint8_t* a_scales;
-    const float* a_s_dec;        // NVFP4 only
+    const float* a_s_dec;        // NVFP4 only: one float, or [M] when a_sdec_rows
     const uint8_t* b;
     const uint8_t* b_scales;
     int b_scale_kind;            // NVFP4: 1 = 1D, 2 = 16x16 tiles
@@ -55,7 +58,8 @@ struct GemmArgs {
     int epi = 0;
     void* d2 = nullptr;
     const uint16_t* aux = nullptr;
-    float* amax_out = nullptr;
+    float* amax_out = nullptr;   // epi 1; may be NULL
+    int a_sdec_rows = 0;         // NVFP4: A carries one outer scale per row
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st);
 int read_and_clear_device_error(cudaStream_t st, int* flag);

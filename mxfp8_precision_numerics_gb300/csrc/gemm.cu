@@ -79,8 +79,9 @@ struct Params {
     const uint8_t* b_sc;
     int64_t sc_ld;             // scale bytes per row (K/16 NVFP4, K/32 MXFP8)
     int b_sc_2d;
-    const float* a_s_dec;
+    const float* a_s_dec;      // one float, or [M] when a_sdec_rows
     const float* b_s_dec;
+    int a_sdec_rows;
     void* d;
     int d_bf16;
     int64_t M, N, K;
@@ -351,7 +352,7 @@ __device__ __forceinline__ void epi_bf16(const Params& p, const uint32_t (&pk)[1
 }
 // The warp's running |GELU| max into amax_out (fp32 bit pattern of the bf16 magnitude).
 __device__ __forceinline__ void epi_flush_amax(const Params& p, uint32_t amax_bits, int lane) {
-    if (p.epi != 1) return;
+    if (p.epi != 1 || !p.amax_out) return;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, o));
     if (lane == 0 && amax_bits) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), amax_bits << 16);
@@ -360,9 +361,10 @@ __device__ __forceinline__ void epi_flush_amax(const Params& p, uint32_t amax_bi
 // Epilogue of one 128 x 256 accumulator: warp w (TMEM lane quarter w) loads rows
 // m0 + 32w + lane, 32 columns at a time, scales by alpha and stores fp32 or bf16.
 __device__ __forceinline__ void store_tile(const Params& p, uint32_t tacc, int warp, int lane, int64_t m0,
-                                           int64_t m_end, int64_t n0, float alpha) {
+                                           int64_t m_end, int64_t n0, float alpha, float b_sd) {
     const int64_t row = m0 + warp * 32 + lane;
     const bool row_ok = row < m_end;
+    if (p.a_sdec_rows) alpha = row_ok ? __fmul_rn(p.a_s_dec[row], b_sd) : 0.0f;   // per-row outer scale of A
     uint32_t amax_bits = 0;
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
@@ -683,8 +685,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const bool ok = mbar_wait(accum, 0);
         tc_fence_after();
         if (ok) {
-            const float alpha = kKind == 0 ? __fmul_rn(p.a_s_dec[0], p.b_s_dec[g]) : 1.0f;
-            store_tile(p, tmem + kAccCol, warp, lane, m0, m_end, n0, alpha);
+            const float b_sd = kKind == 0 ? p.b_s_dec[g] : 1.0f;
+            const float alpha = kKind == 0 && !p.a_sdec_rows ? __fmul_rn(p.a_s_dec[0], b_sd) : 1.0f;
+            store_tile(p, tmem + kAccCol, warp, lane, m0, m_end, n0, alpha, b_sd);
         }
     }
 
@@ -1062,15 +1065,19 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         const int q = warp & 3, h = (warp - 6) >> 2;
         const uint32_t tacc = tmem + kAccCol + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
         const uint32_t empty_leader = leader_addr(tmem_empty);
-        const float alpha = kKind == 0 ? __fmul_rn(p.a_s_dec[0], p.b_s_dec[0]) : 1.0f;
+        const bool rows_sd = kKind == 0 && p.a_sdec_rows;
+        const float b_sd = kKind == 0 ? p.b_s_dec[0] : 1.0f;
+        const float alpha_t = kKind == 0 && !rows_sd ? __fmul_rn(p.a_s_dec[0], b_sd) : 1.0f;
         uint32_t amax_bits = 0;
         for (int ti = 0; ti < my_tiles; ++ti) {
             int64_t m0, n0;
             pair_tile(p, cid + ti * ncl, rank, m0, n0);
-            if (!mbar_wait_idle(accum_full, (uint32_t)ti & 1u)) break;
-            tc_fence_after();
             const int64_t row = m0 + 32 * q + lane;
             const bool row_ok = row < p.M;
+            // per-row outer scale of A: loaded before the wait for the accumulator
+            const float alpha = rows_sd ? (row_ok ? __fmul_rn(p.a_s_dec[row], b_sd) : 0.0f) : alpha_t;
+            if (!mbar_wait_idle(accum_full, (uint32_t)ti & 1u)) break;
+            tc_fence_after();
             const int64_t col0 = n0 + 128 * h;
             if (p.d_bf16) {
                 // bf16 output: each 32-column chunk is rounded to bf16 pairs as soon as it is in
@@ -1194,6 +1201,7 @@ cudaError_t launch_kind(const GemmArgs& a, cudaStream_t st) {
     p.b_sc_2d = (kKind == 0 && a.b_scale_kind == 2) ? 1 : 0;
     p.a_s_dec = a.a_s_dec;
     p.b_s_dec = a.b_s_dec;
+    p.a_sdec_rows = a.a_sdec_rows;
     p.d = a.d;
     p.d_bf16 = a.d_bf16;
     p.epi = a.epi;
@@ -1258,6 +1266,7 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
     p.b_sc_2d = (kKind == 0 && a.b_scale_kind == 2) ? 1 : 0;
     p.a_s_dec = a.a_s_dec;
     p.b_s_dec = a.b_s_dec;
+    p.a_sdec_rows = a.a_sdec_rows;
     p.d = a.d;
     p.d_bf16 = a.d_bf16;
     p.epi = a.epi;
@@ -1305,7 +1314,7 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
 #define FP4Q_PAIR_MIN_STAGES 1
 #endif
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
-    if (a.epi == 1) {   // the epilogue's |GELU| maximum is an atomicMax into a zeroed word
+    if (a.epi == 1 && a.amax_out) {   // the epilogue's |GELU| maximum is an atomicMax into a zeroed word
         const cudaError_t e = cudaMemsetAsync(a.amax_out, 0, sizeof(float), st);
         if (e != cudaSuccess) return e;
     }

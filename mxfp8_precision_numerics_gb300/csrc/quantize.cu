@@ -200,6 +200,192 @@ __global__ void __launch_bounds__(256) quantize_2d_kernel(const uint16_t* __rest
 }
 
 // ---------------------------------------------------------------------------------------
+// 1D quantize with one outer scale per row and, optionally, the Four Over Six block scale
+// (4bit.vizuara.ai §10; "End-to-End 4-Bit Training" (Thinking Machines), 方案细节).
+// One pass over HBM and no amax kernel: a row's blocks are loaded into registers (kHold
+// blocks of 16 per thread, 1, 2 or 4; a longer row reads the rest again, from L2), the row
+// amax is reduced across the row's threads, and the blocks are encoded from registers.
+// A row is handled by W warps (W = 1, 2, 4 or 8), 8 / W rows per 256-thread CTA; thread t
+// of a row owns blocks t, t + 32W, t + 64W, ... so each load instruction of a warp covers
+// 512 contiguous bytes.
+// ---------------------------------------------------------------------------------------
+constexpr int kRowHoldMax = 4;
+
+// Two fp32 values (a packed pair) -> their E2M1 codes (one byte, low nibble = low half, round
+// to nearest even, saturating) and the grid values of those codes as a packed fp32 pair.
+__device__ __forceinline__ uint32_t e2m1x2_roundtrip(uint64_t y2, uint64_t& q2) {
+    uint32_t byte;
+    asm("{.reg .b8 t; .reg .b32 h; .reg .f32 y0, y1, a, b; .reg .f16 l, u;\n\t"
+        "mov.b64 {y0, y1}, %2;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, y1, y0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 h, t;\n\t"
+        "mov.b32 {l, u}, h;\n\t"
+        "cvt.f32.f16 a, l;\n\t"
+        "cvt.f32.f16 b, u;\n\t"
+        "mov.b64 %1, {a, b};\n\t"
+        "cvt.u32.u8 %0, t;}"
+        : "=r"(byte), "=l"(q2) : "l"(y2));
+    return byte;
+}
+
+// The 16 values of a block (8 packed bf16 words) encoded with both Four Over Six candidates
+// (local encode scales se6 and se4): codes c6 / c4 and, for each, the sum of squared
+// distances between the scaled values y and their grid points q. y - q is exact; the squares
+// go into two fused multiply-add chains, one over the even positions and one over the odd
+// (the two halves of packed fp32 pairs), which are added at the end.
+__device__ __forceinline__ void encode16_46(const uint32_t (&w)[8], float se6, float se4, uint2& c6, uint2& c4,
+                                            float& sq6, float& sq4) {
+    uint64_t s6, s4, a6, a4;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(s6) : "f"(se6));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(s4) : "f"(se4));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(a6) : "f"(0.0f));
+    a4 = a6;
+    uint32_t lo6 = 0, hi6 = 0, lo4 = 0, hi4 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint64_t x2, y6, y4, q6, q4, d6, d4;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "r"(w[j] << 16), "r"(w[j] & 0xFFFF0000u));
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y6) : "l"(x2), "l"(s6));
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y4) : "l"(x2), "l"(s4));
+        const uint32_t b6 = e2m1x2_roundtrip(y6, q6), b4 = e2m1x2_roundtrip(y4, q4);
+        asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d6) : "l"(y6), "l"(q6));
+        asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d4) : "l"(y4), "l"(q4));
+        asm("fma.rn.f32x2 %0, %1, %1, %0;" : "+l"(a6) : "l"(d6));
+        asm("fma.rn.f32x2 %0, %1, %1, %0;" : "+l"(a4) : "l"(d4));
+        if (j < 4) {
+            lo6 |= b6 << (8 * j);
+            lo4 |= b4 << (8 * j);
+        } else {
+            hi6 |= b6 << (8 * (j - 4));
+            hi4 |= b4 << (8 * (j - 4));
+        }
+    }
+    float e0, e1;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(e0), "=f"(e1) : "l"(a6));
+    sq6 = __fadd_rn(e0, e1);
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(e0), "=f"(e1) : "l"(a4));
+    sq4 = __fadd_rn(e0, e1);
+    c6 = make_uint2(lo6, hi6);
+    c4 = make_uint2(lo4, hi4);
+}
+
+// Both candidate block scales from one hardware conversion (round to nearest even, saturating
+// at 448: the rule of e4m3_rne_sat): byte 0 for target 6, (amax_b / 6) * s_enc, and byte 1 for
+// target 4, (amax_b / 4) * s_enc; a scale that rounds to zero is raised to the smallest code.
+__device__ __forceinline__ uint32_t scale_codes_46(float amax_b, float s_enc) {
+    const float v6 = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc);
+    const float v4 = __fmul_rn(__fmul_rn(amax_b, 0.25f), s_enc);     // amax_b / 4 is exact
+    uint32_t c;
+    asm("{.reg .b16 t; cvt.rn.satfinite.e4m3x2.f32 t, %1, %2; cvt.u32.u16 %0, t;}" : "=r"(c) : "f"(v4), "f"(v6));
+    return __vmaxu4(c, 0x0101u);
+}
+
+// The low two bytes of c as E4M3 values in fp32 (exact through f16).
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t c, float& lo, float& hi) {
+    asm("{.reg .b16 t; .reg .b32 h; .reg .f16 l, u;\n\t"
+        "cvt.u16.u32 t, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h, t;\n\t"
+        "mov.b32 {l, u}, h;\n\t"
+        "cvt.f32.f16 %0, l;\n\t"
+        "cvt.f32.f16 %1, u;}"
+        : "=f"(lo), "=f"(hi) : "r"(c));
+}
+
+template <bool kFourSix>
+__device__ __forceinline__ void encode_row_block(const uint32_t (&w)[8], float s_enc, float s_dec,
+                                                 uint8_t* crow, uint8_t* srow, int64_t b) {
+    const float amax_b = absmax16(w);
+    uint32_t sb;
+    uint2 c;
+    if (!kFourSix) {
+        sb = block_scale(amax_b, s_enc);
+        c = encode16<true>(w, block_encode_scale(sb, s_dec));
+    } else {
+        const uint32_t sc = scale_codes_46(amax_b, s_enc);
+        float S6, S4;
+        e4m3x2_to_f32(sc, S6, S4);
+        uint2 c4;
+        float sq6, sq4;
+        encode16_46(w, __frcp_rn(__fmul_rn(S6, s_dec)), __frcp_rn(__fmul_rn(S4, s_dec)), c, c4, sq6, sq4);
+        const float e6 = __fmul_rn(sq6, __fmul_rn(S6, S6)), e4 = __fmul_rn(sq4, __fmul_rn(S4, S4));
+        sb = sc & 0xFFu;
+        if (e4 < e6) {   // a tie keeps the ordinary scale
+            sb = (sc >> 8) & 0xFFu;
+            c = c4;
+        }
+    }
+    reinterpret_cast<uint2*>(crow)[b] = c;
+    srow[b] = (uint8_t)sb;
+}
+
+__device__ __forceinline__ void load_block(const uint16_t* xr, int64_t b, bool stream, uint32_t (&w)[8]) {
+    const uint4* src = reinterpret_cast<const uint4*>(xr + b * 16);
+    const uint4 p = stream ? __ldcs(src) : __ldg(src), q = stream ? __ldcs(src + 1) : __ldg(src + 1);
+    w[0] = p.x; w[1] = p.y; w[2] = p.z; w[3] = p.w;
+    w[4] = q.x; w[5] = q.y; w[6] = q.z; w[7] = q.w;
+}
+
+template <bool kFourSix, int kHold>
+__global__ void __launch_bounds__(256) quantize_1d_rows_kernel(const uint16_t* __restrict__ x,
+                                                               int64_t rows, int64_t cols, int64_t ld, int W,
+                                                               uint8_t* __restrict__ codes,
+                                                               uint8_t* __restrict__ scales,
+                                                               float* __restrict__ s_dec_rows) {
+    const int T = 32 * W;
+    const int lr = threadIdx.x / T, t = threadIdx.x - lr * T;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (8 / W) + lr;
+    const bool row_ok = row < rows;
+    const int64_t nb = cols >> 4;
+    const uint16_t* xr = x + (row_ok ? row : 0) * ld;
+
+    uint32_t w[kHold][8];
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int j = 0; j < kHold; ++j) {
+        const int64_t b = t + (int64_t)j * T;
+        if (row_ok && b < nb) {
+            load_block(xr, b, true, w[j]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[j][k] = 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m2 = __vmaxu2(m2, w[j][k] & 0x7FFF7FFFu);
+    }
+    for (int64_t b = t + (int64_t)kHold * T; row_ok && b < nb; b += T) {   // rows longer than held
+        uint32_t v[8];
+        load_block(xr, b, false, v);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m2 = __vmaxu2(m2, v[k] & 0x7FFF7FFFu);
+    }
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    __shared__ uint32_t red[8];
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    for (int i = 0; i < W; ++i) m = max(m, red[lr * W + i]);
+    if (!row_ok) return;
+    float s_enc, s_dec;
+    global_scales(__uint_as_float(m << 16), s_enc, s_dec);   // |bf16| bits << 16 = its fp32 pattern
+
+    uint8_t* crow = codes + row * (cols >> 1);
+    uint8_t* srow = scales + row * nb;
+#pragma unroll
+    for (int j = 0; j < kHold; ++j) {
+        const int64_t b = t + (int64_t)j * T;
+        if (b < nb) encode_row_block<kFourSix>(w[j], s_enc, s_dec, crow, srow, b);
+    }
+    for (int64_t b = t + (int64_t)kHold * T; b < nb; b += T) {
+        uint32_t v[8];
+        load_block(xr, b, true, v);
+        encode_row_block<kFourSix>(v, s_enc, s_dec, crow, srow, b);
+    }
+    if (t == 0) s_dec_rows[row] = s_dec;
+}
+
+// ---------------------------------------------------------------------------------------
 // host launchers (validated by the C-ABI layer)
 // ---------------------------------------------------------------------------------------
 static int grid_for(int64_t work_items, int threads) {
@@ -245,6 +431,41 @@ cudaError_t launch_quantize_2d(const uint16_t* w, int64_t rows, int64_t cols, in
     else
         quantize_2d_kernel<false><<<grid, 256, 0, st>>>(w, rows, cols, ld, batch_stride, amax, codes,
                                                         tile_scales, s_dec);
+    return cudaGetLastError();
+}
+
+// Warps per row and blocks held per thread: up to 4 blocks per thread (a load of 128 bytes
+// per thread in flight before the row's amax is known) and as few warps as cover the row, up
+// to 8; a row longer than 8 warps x 4 blocks reads the rest twice.
+void rows_shape(int64_t cols, int& W, int& hold) {
+    const int64_t nb = cols / 16;
+    W = 1;
+    while (W < 8 && (int64_t)32 * W * kRowHoldMax < nb) W *= 2;
+    hold = 1;
+    while (hold < kRowHoldMax && (int64_t)32 * W * hold < nb) hold *= 2;
+}
+
+template <bool kFourSix>
+static void launch_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int W, int hold,
+                        uint8_t* codes, uint8_t* scales, float* s_dec_rows, unsigned g, cudaStream_t st) {
+    if (hold == 1)
+        quantize_1d_rows_kernel<kFourSix, 1><<<g, 256, 0, st>>>(x, rows, cols, ld, W, codes, scales, s_dec_rows);
+    else if (hold == 2)
+        quantize_1d_rows_kernel<kFourSix, 2><<<g, 256, 0, st>>>(x, rows, cols, ld, W, codes, scales, s_dec_rows);
+    else
+        quantize_1d_rows_kernel<kFourSix, 4><<<g, 256, 0, st>>>(x, rows, cols, ld, W, codes, scales, s_dec_rows);
+}
+
+cudaError_t launch_quantize_1d_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int four_six,
+                                    uint8_t* codes, uint8_t* scales, float* s_dec_rows, cudaStream_t st) {
+    int W, hold;
+    rows_shape(cols, W, hold);
+    const int64_t g = (rows + (8 / W) - 1) / (8 / W);
+    if (g > 2147483647) return cudaErrorInvalidValue;
+    if (four_six)
+        launch_rows<true>(x, rows, cols, ld, W, hold, codes, scales, s_dec_rows, (unsigned)g, st);
+    else
+        launch_rows<false>(x, rows, cols, ld, W, hold, codes, scales, s_dec_rows, (unsigned)g, st);
     return cudaGetLastError();
 }
 

@@ -12,10 +12,12 @@
 // Kernels
 //   requant_rows_kernel  (transpose = 0): one thread per 32-value output block, read
 //                        straight from HBM (bf16: 64 B, NVFP4: 16 B codes + 2 scales).
-//   requant_t_kernel     (transpose = 1): a CTA dequantizes a 64 x 64 input tile into shared
-//                        memory (fp32, padded rows), then each thread reads one input column
-//                        segment of 32 = one output block, transforms, quantizes and writes
-//                        32 bytes of the output row.
+//   requant_t_kernel     (transpose = 1): persistent CTAs walk 64 x 128 input tiles, staged
+//                        raw in shared memory one tile ahead; two lanes share one 32-value
+//                        output block (one transform group each), see below.
+// Input kinds: bf16; NVFP4 with 1D or 16x16 tile scales and one outer scale; NVFP4 with 1D
+// scales and one outer scale per input row (the per-token activation form of
+// 4bit.vizuara.ai §10), where each dequantized value takes its own row's s_dec.
 #include "fp4q_common.cuh"
 #include "fp4q_internal.h"
 
@@ -90,7 +92,7 @@ template <int kKind, bool kRht, bool kSR>
 __global__ void __launch_bounds__(256) requant_rows_kernel(RequantArgs a) {
     const int64_t nb = a.cols >> 5;
     const int64_t total = a.rows * nb;
-    const float s_dec = (kKind == 0) ? 1.0f : *a.in_s_dec;
+    const float s_dec_t = (kKind == 0 || kKind == 3) ? 1.0f : *a.in_s_dec;   // kind 3: per row
     // sign masks of the transform positions, packed like the input words
     uint32_t bm[8], nm0 = 0, nm1 = 0;
 #pragma unroll
@@ -117,7 +119,8 @@ __global__ void __launch_bounds__(256) requant_rows_kernel(RequantArgs a) {
             const uint4 c = __ldcs(reinterpret_cast<const uint4*>(
                 static_cast<const uint8_t*>(a.in) + r * (a.cols >> 1) + j * 16));
             uint32_t s0, s1;
-            if (kKind == 1) {
+            const float s_dec = kKind == 3 ? a.in_s_dec[r] : s_dec_t;
+            if (kKind != 2) {
                 s0 = a.in_scales[r * (a.cols >> 4) + 2 * j];
                 s1 = a.in_scales[r * (a.cols >> 4) + 2 * j + 1];
             } else {
@@ -217,13 +220,14 @@ template <int kKind, bool kRht, bool kSR>
 __global__ void __launch_bounds__(kTThreads) requant_t_kernel(RequantArgs a, int tiles_c, int n_tiles) {
     __shared__ __align__(16) uint8_t stage[2][TStage<kKind>::kBytes];
     __shared__ uint32_t sct[2][kKind == 0 ? 1 : kTR][8];   // per input row: f16x2 scales, signs folded
+    __shared__ float sdr[2][kKind == 3 ? kTR : 1];          // kind 3: per input row outer scale
     const int tid = threadIdx.x;
     const int p = tid >> 2, grp = tid & 3, hb = grp & 1;
-    const float s_dec = (kKind == 0) ? 1.0f : *a.in_s_dec;
+    const float s_dec = (kKind == 0 || kKind == 3) ? 1.0f : *a.in_s_dec;
     const int64_t sc_ld = a.cols >> 4;
 
     // cp.async of tile `tile` into buffer `buf`; block scales of the tile into `sreg`
-    auto issue = [&](int tile, int buf, uint32_t (&sreg)[2]) {
+    auto issue = [&](int tile, int buf, uint32_t (&sreg)[2], float& sdreg) {
         const int tr = tile / tiles_c, tc = tile - tr * tiles_c;
         const int64_t r0 = (int64_t)tr * kTR, c0 = (int64_t)tc * kTC;
         const uint32_t base = (uint32_t)__cvta_generic_to_shared(&stage[buf][0]);
@@ -253,6 +257,7 @@ __global__ void __launch_bounds__(kTThreads) requant_t_kernel(RequantArgs a, int
                 if (grow < a.rows && gcol < sc_ld)
                     sreg[i] = a.in_scales[(kKind == 2 ? (grow >> 4) : grow) * sc_ld + gcol];
             }
+            if (kKind == 3 && tid < kTR) sdreg = r0 + tid < a.rows ? a.in_s_dec[r0 + tid] : 0.0f;
         }
         cp_async_commit();
     };
@@ -260,7 +265,8 @@ __global__ void __launch_bounds__(kTThreads) requant_t_kernel(RequantArgs a, int
     int tile = blockIdx.x;
     if (tile >= n_tiles) return;
     uint32_t sreg[2] = {0, 0};
-    issue(tile, 0, sreg);
+    float sdreg = 0.0f;
+    issue(tile, 0, sreg, sdreg);
     for (int it = 0; tile < n_tiles; ++it, tile += gridDim.x) {
         const int buf = it & 1;
         if (kKind != 0) {
@@ -274,10 +280,11 @@ __global__ void __launch_bounds__(kTThreads) requant_t_kernel(RequantArgs a, int
                 if (kRht) h ^= ((a.rht_signs >> (srow & 15)) & 1u) * 0x80008000u;
                 sct[buf][srow][blk ^ (2 * ((srow >> 4) & 3))] = h;
             }
+            if (kKind == 3 && tid < kTR) sdr[buf][tid] = sdreg;
         }
         const int next = tile + gridDim.x;
         if (next < n_tiles) {
-            issue(next, buf ^ 1, sreg);
+            issue(next, buf ^ 1, sreg, sdreg);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
@@ -310,10 +317,12 @@ __global__ void __launch_bounds__(kTThreads) requant_t_kernel(RequantArgs a, int
             const uint8_t* src = &stage[buf][0] + (16 * grp) * 64 + (p ^ (16 * grp));
             const uint32_t* sc = &sct[buf][16 * grp][(p >> 3) ^ (2 * grp)];
             uint32_t h[16];
+            float sd[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 h[k] = e2m1x2_to_f16x2(src[k * 64]);
                 asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[k]) : "r"(sc[k * 8]));
+                sd[k] = kKind == 3 ? sdr[buf][16 * grp + k] : s_dec;
             }
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
@@ -324,7 +333,7 @@ __global__ void __launch_bounds__(kTThreads) requant_t_kernel(RequantArgs a, int
                     float f;
                     asm("{.reg .f16 l, u; mov.b32 {l, u}, %1; cvt.f32.f16 %0, l;}"
                         : "=f"(f) : "r"(__byte_perm(h[k], 0u, sel)));
-                    v[k] = __fmul_rn(f, s_dec);
+                    v[k] = __fmul_rn(f, sd[k]);
                 }
                 const int64_t oidx = (orow + half) * a.rows + ocol + 16 * hb;
                 mx_encode_half<kRht, kSR>(v, valid, a.seed, a.tag, (uint64_t)oidx, a.out_e4m3 + oidx,
@@ -379,7 +388,7 @@ static void launch_requant_t(const RequantArgs& a, cudaStream_t st) {
     if (a.transpose) {
         const int64_t tiles_c = (a.cols + kTC - 1) / kTC, tiles_r = (a.rows + kTR - 1) / kTR;
         const int64_t n_tiles = tiles_c * tiles_r;
-        static int per_sm[3][2][2] = {};
+        static int per_sm[4][2][2] = {};
         int& occ = per_sm[kKind][kRht ? 1 : 0][kSR ? 1 : 0];
         if (occ <= 0) {
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, requant_t_kernel<kKind, kRht, kSR>, kTThreads, 0) !=
@@ -415,7 +424,8 @@ cudaError_t launch_requant(const RequantArgs& a, cudaStream_t st) {
     switch (a.in_kind) {
         case 0: launch_requant_k<0>(a, st); break;
         case 1: launch_requant_k<1>(a, st); break;
-        default: launch_requant_k<2>(a, st); break;
+        case 2: launch_requant_k<2>(a, st); break;
+        default: launch_requant_k<3>(a, st); break;
     }
     return cudaGetLastError();
 }

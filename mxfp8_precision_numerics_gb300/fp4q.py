@@ -19,7 +19,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfp4q.so")
 
 OK, ERR_NULL, ERR_ALIGN, ERR_SHAPE, ERR_ARG, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = range(8)
-IN_BF16, IN_NVFP4_1D, IN_NVFP4_2D = 0, 1, 2
+IN_BF16, IN_NVFP4_1D, IN_NVFP4_2D, IN_NVFP4_1D_ROWS = 0, 1, 2, 3
 RNE, SR = 0, 1
 F32, BF16 = 0, 1
 SCALE_1D, SCALE_2D = 1, 2
@@ -45,6 +45,7 @@ _SIGS = {
     "fp4q_status_str": (ctypes.c_char_p, [_int]),
     "fp4q_version": (_int, []),
     "fp4q_quantize_1d": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "fp4q_quantize_1d_rows": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _vp, _vp, _vp]),
     "fp4q_quantize_2d": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "fp4q_quantize_2d_noalloc": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
     "fp4q_requant_t_mxfp8_sr": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _int, _u32, _int, _u64,
@@ -52,8 +53,12 @@ _SIGS = {
     "fp4q_rht16": (_int, [_vp, _int, _vp, _i64, _i64, _u32, _vp]),
     "fp4q_gemm_nvfp4": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _int, _i64, _i64, _i64, _int,
                                ctypes.POINTER(ctypes.c_int64), _vp]),
+    "fp4q_gemm_nvfp4_rows": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _int, _i64, _i64, _i64, _int,
+                                    _vp, _vp]),
     "fp4q_gemm_mxfp8": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp]),
     "fp4q_gemm_nvfp4_gelu": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "fp4q_gemm_nvfp4_gelu_rows": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
+                                         _vp]),
     "fp4q_gemm_mxfp8_dgelu": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "fp4q_device_status": (_int, [_vp]),
 }
@@ -97,6 +102,11 @@ def fp4q_quantize_1d(x, rows, cols, ld, amax_in, amax_ws, codes, scales, s_dec_o
                                  _ptr(scales), _ptr(s_dec_out), _stream(stream)), "fp4q_quantize_1d")
 
 
+def fp4q_quantize_1d_rows(x, rows, cols, ld, four_six, codes, scales, s_dec_rows, stream=None):
+    _check(_lib.fp4q_quantize_1d_rows(_ptr(x), rows, cols, ld, int(four_six), _ptr(codes), _ptr(scales),
+                                      _ptr(s_dec_rows), _stream(stream)), "fp4q_quantize_1d_rows")
+
+
 def fp4q_quantize_2d(w, rows, cols, ld, batch, batch_stride, amax_in, amax_ws, codes, tile_scales,
                      s_dec_out, stream=None):
     _check(_lib.fp4q_quantize_2d(_ptr(w), rows, cols, ld, batch, batch_stride, _ptr(amax_in),
@@ -126,15 +136,29 @@ def fp4q_rht16(inp, in_dtype, out, rows, cols, signs, stream=None):
            "fp4q_rht16")
 
 
+def _offsets(group_row_offsets):
+    if group_row_offsets is None:
+        return None, None
+    arr = (ctypes.c_int64 * len(group_row_offsets))(*[int(v) for v in group_row_offsets])
+    return arr, ctypes.cast(arr, ctypes.POINTER(ctypes.c_int64))
+
+
 def fp4q_gemm_nvfp4(a, a_scales, a_s_dec, b, b_scales, b_scale_kind, b_s_dec, d, d_dtype, M, N, K,
                     groups=1, group_row_offsets=None, stream=None):
-    offs = None
-    if group_row_offsets is not None:
-        arr = (ctypes.c_int64 * len(group_row_offsets))(*[int(v) for v in group_row_offsets])
-        offs = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int64))
+    keep, offs = _offsets(group_row_offsets)
     _check(_lib.fp4q_gemm_nvfp4(_ptr(a), _ptr(a_scales), _ptr(a_s_dec), _ptr(b), _ptr(b_scales),
                                 b_scale_kind, _ptr(b_s_dec), _ptr(d), d_dtype, M, N, K, groups, offs,
                                 _stream(stream)), "fp4q_gemm_nvfp4")
+    del keep
+
+
+def fp4q_gemm_nvfp4_rows(a, a_scales, a_s_dec_rows, b, b_scales, b_scale_kind, b_s_dec, d, d_dtype, M, N, K,
+                         groups=1, group_row_offsets=None, stream=None):
+    keep, offs = _offsets(group_row_offsets)
+    _check(_lib.fp4q_gemm_nvfp4_rows(_ptr(a), _ptr(a_scales), _ptr(a_s_dec_rows), _ptr(b), _ptr(b_scales),
+                                     b_scale_kind, _ptr(b_s_dec), _ptr(d), d_dtype, M, N, K, groups, offs,
+                                     _stream(stream)), "fp4q_gemm_nvfp4_rows")
+    del keep
 
 
 def fp4q_gemm_mxfp8(a, a_scales, b, b_scales, d, d_dtype, M, N, K, stream=None):
@@ -147,6 +171,14 @@ def fp4q_gemm_nvfp4_gelu(a, a_scales, a_s_dec, b, b_scales, b_scale_kind, b_s_de
     _check(_lib.fp4q_gemm_nvfp4_gelu(_ptr(a), _ptr(a_scales), _ptr(a_s_dec), _ptr(b), _ptr(b_scales),
                                      b_scale_kind, _ptr(b_s_dec), _ptr(h_out), _ptr(act_out), _ptr(act_amax),
                                      M, N, K, _stream(stream)), "fp4q_gemm_nvfp4_gelu")
+
+
+def fp4q_gemm_nvfp4_gelu_rows(a, a_scales, a_s_dec_rows, b, b_scales, b_scale_kind, b_s_dec, h_out, act_out,
+                              act_amax, M, N, K, stream=None):
+    _check(_lib.fp4q_gemm_nvfp4_gelu_rows(_ptr(a), _ptr(a_scales), _ptr(a_s_dec_rows), _ptr(b), _ptr(b_scales),
+                                          b_scale_kind, _ptr(b_s_dec), _ptr(h_out), _ptr(act_out),
+                                          _ptr(act_amax), M, N, K, _stream(stream)),
+           "fp4q_gemm_nvfp4_gelu_rows")
 
 
 def fp4q_gemm_mxfp8_dgelu(a, a_scales, b, b_scales, h, dh_out, M, N, K, stream=None):
@@ -174,6 +206,18 @@ def quantize_1d(x, amax_in=None, stream=None):
     amax_ws = None if amax_in is not None else _empty((1,), torch.float32, dev)
     fp4q_quantize_1d(x, rows, cols, x.stride(0), amax_in, amax_ws, codes, scales, s_dec, stream)
     return codes, scales, s_dec, (amax_in if amax_in is not None else amax_ws)
+
+
+def quantize_1d_rows(x, four_six=True, stream=None):
+    """bf16 [rows, cols] -> (codes u8 [rows, cols/2], scales u8 [rows, cols/16],
+    s_dec_rows f32 [rows]): one outer scale per row, 4/6 block scales if four_six."""
+    rows, cols = x.shape
+    dev = x.device
+    codes = _empty((rows, cols // 2), torch.uint8, dev)
+    scales = _empty((rows, cols // 16), torch.uint8, dev)
+    s_dec = _empty((rows,), torch.float32, dev)
+    fp4q_quantize_1d_rows(x, rows, cols, x.stride(0), four_six, codes, scales, s_dec, stream)
+    return codes, scales, s_dec
 
 
 def quantize_2d(w, amax_in=None, stream=None):
@@ -221,6 +265,29 @@ def gemm_nvfp4(a, a_scales, a_s_dec, b, b_scales, b_scale_kind, b_s_dec, out_dty
                     BF16 if out_dtype == torch.bfloat16 else F32, M, N, K, groups, group_row_offsets,
                     stream)
     return d
+
+
+def gemm_nvfp4_rows(a, a_scales, a_s_dec_rows, b, b_scales, b_scale_kind, b_s_dec, out_dtype=torch.float32,
+                    groups=1, group_row_offsets=None, stream=None):
+    """gemm_nvfp4 with one outer scale per row of A (a_s_dec_rows f32 [M])."""
+    M, K = a.shape[0], a.shape[1] * 2
+    N = b.shape[-2]
+    d = _empty((M, N), out_dtype, a.device)
+    fp4q_gemm_nvfp4_rows(a, a_scales, a_s_dec_rows, b, b_scales, b_scale_kind, b_s_dec, d,
+                         BF16 if out_dtype == torch.bfloat16 else F32, M, N, K, groups, group_row_offsets,
+                         stream)
+    return d
+
+
+def gemm_nvfp4_gelu_rows(a, a_scales, a_s_dec_rows, b, b_scales, b_scale_kind, b_s_dec, stream=None):
+    """-> (h, act): gemm_nvfp4_gelu with one outer scale per row of A, no tensor amax."""
+    M, K = a.shape[0], a.shape[1] * 2
+    N = b.shape[-2]
+    h = _empty((M, N), torch.bfloat16, a.device)
+    act = _empty((M, N), torch.bfloat16, a.device)
+    fp4q_gemm_nvfp4_gelu_rows(a, a_scales, a_s_dec_rows, b, b_scales, b_scale_kind, b_s_dec, h, act, None,
+                              M, N, K, stream)
+    return h, act
 
 
 def gemm_nvfp4_gelu(a, a_scales, a_s_dec, b, b_scales, b_scale_kind, b_s_dec, stream=None):

@@ -9,6 +9,10 @@ as it is for dgrad and transposed (with the 16-point RHT) for wgrad; the saved N
 weight and activation are dequantized, transposed and re-quantized to MXFP8 with SR
 (the activation with the RHT, the weight without). dgrad sums over N, wgrad over tokens.
 
+Activations take either one outer scale per tensor (the NVFP4 paper's recipe) or, with
+outer="row", one per token row plus the Four Over Six block-scale choice (4bit.vizuara.ai §10:
+QLinearFn quantizes x with outer="row", four_six=True and w with outer="tensor").
+
 GELU between the two linear layers of the MLP block (exact erf form, bf16) is fused into the
 epilogues of the GEMMs around it: the first layer's NVFP4 GEMM writes h, GELU(h) and
 max|GELU(h)| (which the second layer's quantize takes as its amax), and the second layer's
@@ -29,23 +33,35 @@ class SavedLinear:
     M: int
     K: int
     N: int
+    x_rows: bool = False   # xq's s_dec holds one outer scale per row
 
 
-def linear_forward(x, w=None, wq=None, out_dtype=torch.bfloat16, stream=None, x_amax=None, gelu=False):
+def linear_forward(x, w=None, wq=None, out_dtype=torch.bfloat16, stream=None, x_amax=None, gelu=False,
+                   outer="tensor", four_six=True):
     """y = x w^T on NVFP4 operands. x: [M, K] bf16; w: [N, K] bf16 (or wq precomputed).
-    x_amax: max|x| if already known (device float), else the quantizer computes it.
-    gelu=True returns ((h, GELU(h), max|GELU(h)|), saved) instead of (y, saved)."""
+    outer: "tensor" (one outer scale for x; x_amax = max|x| if already known, as a device
+    float) or "row" (one per token row, with 4/6 block scales if four_six).
+    gelu=True returns ((h, GELU(h), max|GELU(h)|), saved) instead of (y, saved); with
+    outer="row" it returns ((h, GELU(h)), saved)."""
+    if outer not in ("tensor", "row"):
+        raise ValueError(f"outer must be 'tensor' or 'row', not {outer!r}")
+    rows = outer == "row"
     M, K = x.shape
-    xc, xs, xsd, _ = F.quantize_1d(x, amax_in=x_amax, stream=stream)
+    if rows:
+        xc, xs, xsd = F.quantize_1d_rows(x, four_six, stream=stream)
+    else:
+        xc, xs, xsd, _ = F.quantize_1d(x, amax_in=x_amax, stream=stream)
     if wq is None:
         wc, ws, wsd, _ = F.quantize_2d(w, stream=stream)
         wq = (wc, ws, wsd)
     wc, ws, wsd = wq
     N = wc.shape[0]
-    saved = SavedLinear((xc, xs, xsd), wq, M, K, N)
+    saved = SavedLinear((xc, xs, xsd), wq, M, K, N, rows)
     if gelu:
-        return F.gemm_nvfp4_gelu(xc, xs, xsd, wc, ws, F.SCALE_2D, wsd, stream=stream), saved
-    y = F.gemm_nvfp4(xc, xs, xsd, wc, ws, F.SCALE_2D, wsd, out_dtype, stream=stream)
+        fn = F.gemm_nvfp4_gelu_rows if rows else F.gemm_nvfp4_gelu
+        return fn(xc, xs, xsd, wc, ws, F.SCALE_2D, wsd, stream=stream), saved
+    fn = F.gemm_nvfp4_rows if rows else F.gemm_nvfp4
+    y = fn(xc, xs, xsd, wc, ws, F.SCALE_2D, wsd, out_dtype, stream=stream)
     return y, saved
 
 
@@ -65,13 +81,19 @@ def linear_backward(dy, saved, seed, rht_signs, dx_dtype=torch.bfloat16, stream=
         dx = F.gemm_mxfp8(g[0], g[1], wt[0], wt[1], dx_dtype, stream)
     # wgrad: dw[n, k] = sum_m dy[m, n] x[m, k]   (blocks and RHT along tokens)
     gt = F.requant_mxfp8(F.IN_BF16, dy, None, None, M, N, 1, 1, rht_signs, rounding, seed, F.TAG_DY_T, stream)
-    xt = F.requant_mxfp8(F.IN_NVFP4_1D, xc, xs, xsd, M, K, 1, 1, rht_signs, rounding, seed, F.TAG_XT, stream)
+    x_kind = F.IN_NVFP4_1D_ROWS if saved.x_rows else F.IN_NVFP4_1D
+    xt = F.requant_mxfp8(x_kind, xc, xs, xsd, M, K, 1, 1, rht_signs, rounding, seed, F.TAG_XT, stream)
     dw = F.gemm_mxfp8(gt[0], gt[1], xt[0], xt[1], torch.float32, stream)
     return dx, dw
 
 
-def mlp_forward(x, w1, w2, stream=None):
-    """GPT MLP block: y = gelu(x w1^T) w2^T. x [M, D], w1 [Fh, D], w2 [D, Fh]."""
+def mlp_forward(x, w1, w2, stream=None, outer="tensor"):
+    """GPT MLP block: y = gelu(x w1^T) w2^T. x [M, D], w1 [Fh, D], w2 [D, Fh].
+    outer="row": both activations (x and GELU(h)) per token row with 4/6 block scales."""
+    if outer == "row":
+        (h, a), s1 = linear_forward(x, w1, stream=stream, gelu=True, outer="row")
+        y, s2 = linear_forward(a, w2, stream=stream, outer="row")
+        return y, (h, s1, s2)
     (h, a, a_amax), s1 = linear_forward(x, w1, stream=stream, gelu=True)
     y, s2 = linear_forward(a, w2, stream=stream, x_amax=a_amax)
     return y, (h, s1, s2)
@@ -91,9 +113,10 @@ def mlp_gemm_flops(M, D, Fh):
     return 6 * 2 * M * D * Fh
 
 
-def mlp_kernel_launches():
+def mlp_kernel_launches(outer="tensor"):
     """libfp4q kernels one mlp_forward + mlp_backward launches (counted from the calls):
     forward: amax + quantize_1d of x, quantize_1d of GELU(h) (its amax comes from the GELU
-    GEMM's epilogue), 2 x (amax + quantize_2d of a weight), 2 NVFP4 GEMMs = 9;
+    GEMM's epilogue), 2 x (amax + quantize_2d of a weight), 2 NVFP4 GEMMs = 9 (outer="row":
+    one per-row quantize for each activation, no activation amax: 8);
     backward: 2 x (4 requant + 2 MXFP8 GEMMs) = 12."""
-    return 21
+    return 20 if outer == "row" else 21

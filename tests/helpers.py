@@ -1,5 +1,9 @@
 """Shared assertions for the parity tests."""
+import math
+
 import numpy as np
+
+_erfc = np.vectorize(math.erfc)
 
 # GEMM tolerance stated for the fp32-output GEMMs: max|diff| <= 1e-3 max|ref|, relative
 # Frobenius error <= 1e-4, against the float64 product of the exactly dequantized operands.
@@ -47,3 +51,29 @@ def assert_bf16_rounding_of(got_bf16_u16, ref, what):
     tol = np.maximum(ulp, GEMM_MAXDIFF_REL * np.max(np.abs(ref)))
     bad = err > tol
     assert not bad.any(), f"{what}: {int(bad.sum())} bf16 outputs off by more than one ulp"
+
+
+def phi64(x):
+    """Standard normal cdf as erfc(-x/sqrt 2)/2: no cancellation in the negative tail."""
+    return 0.5 * _erfc(-np.asarray(x, dtype=np.float64) / math.sqrt(2.0))
+
+
+def gelu64(x):
+    x = np.asarray(x, dtype=np.float64)
+    return x * phi64(x)
+
+
+def gelu_grad64(x):
+    x = np.asarray(x, dtype=np.float64)
+    return phi64(x) + x * np.exp(-0.5 * x * x) / math.sqrt(2.0 * math.pi)
+
+
+def assert_bf16_near(got_u16, want64, ulps, what):
+    """bf16 results within `ulps` bf16 ulps of a float64 value (the epilogue's GELU is not
+    correctly rounded, so the last bf16 bit may differ)."""
+    got = bf16_values(got_u16).astype(np.float64)
+    want = np.asarray(want64, dtype=np.float64)
+    tol = ulps * np.maximum(np.abs(want), 2.0 ** -126) * 2.0 ** -7 + 2.0 ** -133
+    bad = np.abs(got - want) > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} beyond {ulps} bf16 ulp; first "
+                           f"got {got[bad][0]!r} want {want[bad][0]!r}")

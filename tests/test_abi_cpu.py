@@ -66,7 +66,8 @@ def test_validation_rejects_bad_arguments_without_touching_cuda(F):
     assert L.fp4q_quantize_2d(p, 32, 32, 32, 2, 16, n, p, p, p, p, n) == F.ERR_SHAPE  # overlapping batch
     assert L.fp4q_quantize_2d(p, 32, 32, 32, 1, 0, n, p, n, p, p, n) == F.ERR_NULL
     # requant
-    assert L.fp4q_requant_t_mxfp8_sr(3, p, p, p, 32, 32, 1, 0, 0, 1, 0, 0, p, p, n) == F.ERR_ARG
+    assert L.fp4q_requant_t_mxfp8_sr(4, p, p, p, 32, 32, 1, 0, 0, 1, 0, 0, p, p, n) == F.ERR_ARG
+    assert L.fp4q_requant_t_mxfp8_sr(3, p, p, n, 32, 32, 1, 0, 0, 1, 0, 0, p, p, n) == F.ERR_NULL  # s_dec rows
     assert L.fp4q_requant_t_mxfp8_sr(0, p, n, n, 32, 32, 2, 0, 0, 1, 0, 0, p, p, n) == F.ERR_ARG
     assert L.fp4q_requant_t_mxfp8_sr(0, p, n, n, 32, 32, 1, 0, 0, 2, 0, 0, p, p, n) == F.ERR_ARG
     assert L.fp4q_requant_t_mxfp8_sr(0, p, n, n, 32, 32, 1, 1, 1 << 16, 1, 0, 0, p, p, n) == F.ERR_ARG
@@ -102,6 +103,26 @@ def test_validation_rejects_bad_arguments_without_touching_cuda(F):
     assert ge(p, p, p, p, p, 3, p, p, p, p, 128, 256, 256, n) == F.ERR_ARG            # scale kind
     assert ge(p, p, p, p, p, 2, p, p, p, p, 128, 256, 200, n) == F.ERR_SHAPE          # K % 256
     assert ge(p, p, p, p, p, 2, p, p, q, p, 128, 256, 256, n) == F.ERR_ALIGN          # h_out
+    gr = L.fp4q_gemm_nvfp4_gelu_rows
+    assert gr(p, p, n, p, p, 2, p, p, p, n, 128, 256, 256, n) == F.ERR_NULL           # no row scales
+    assert gr(p, p, p, p, p, 2, p, p, p, ctypes.c_void_p(18), 128, 256, 256, n) == F.ERR_ALIGN
+    assert gr(p, p, p, p, p, 2, p, p, p, p, 128, 256, 200, n) == F.ERR_SHAPE          # K % 256
+    # act_amax may be NULL in the per-row form: past validation, no GPU here
+    assert gr(p, p, p, p, p, 2, p, p, p, n, 128, 256, 256, n) in (F.ERR_CUDA, F.ERR_UNSUPPORTED)
+    r = L.fp4q_gemm_nvfp4_rows
+    assert r(p, p, n, p, p, 1, p, p, 0, 128, 256, 256, 1, None, n) == F.ERR_NULL
+    assert r(p, p, p, p, p, 3, p, p, 0, 128, 256, 256, 1, None, n) == F.ERR_ARG
+    assert r(p, p, p, p, p, 1, p, p, 0, 128, 256, 128, 1, None, n) == F.ERR_SHAPE
+    # quantize_1d_rows
+    qr = L.fp4q_quantize_1d_rows
+    assert qr(p, 16, 32, 32, 2, p, p, p, n) == F.ERR_ARG                               # four_six
+    assert qr(p, 16, 32, 32, 1, p, p, n, n) == F.ERR_NULL
+    assert qr(p, 16, 40, 40, 1, p, p, p, n) == F.ERR_SHAPE
+    assert qr(p, 0, 32, 32, 1, p, p, p, n) == F.ERR_SHAPE
+    assert qr(p, 16, 32, 16, 1, p, p, p, n) == F.ERR_SHAPE                             # ld < cols
+    assert qr(q, 16, 32, 32, 1, p, p, p, n) == F.ERR_ALIGN
+    assert qr(p, 16, 32, 36, 1, p, p, p, n) == F.ERR_ALIGN                             # ld % 8
+    assert qr(p, 16, 32, 32, 1, p, p, p, n) in (F.ERR_CUDA, F.ERR_UNSUPPORTED)        # valid, no GPU
     dg = L.fp4q_gemm_mxfp8_dgelu
     assert dg(p, p, p, p, n, p, 128, 256, 128, n) == F.ERR_NULL                        # no h
     assert dg(p, p, p, p, p, p, 128, 250, 128, n) == F.ERR_SHAPE                       # N % 16

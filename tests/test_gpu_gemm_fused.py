@@ -3,18 +3,14 @@ fp4q_gemm_mxfp8_dgelu): the GEMM part against the oracle's float64 product (one 
 as for every bf16 GEMM output) and bit-identical to the plain GEMM's bf16 output; the
 activation part against GELU(x) = x Phi(x) and GELU'(x) = Phi(x) + x phi(x) evaluated in
 float64 on the very bf16 values the epilogue started from; the |GELU| maximum exactly."""
-import math
-
 import numpy as np
 import pytest
 import torch
 
-from helpers import assert_bf16_rounding_of, bf16_values
+from helpers import assert_bf16_near, assert_bf16_rounding_of, bf16_values, gelu64, gelu_grad64
 from mxfp8_precision_numerics_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
-
-_erfc = np.vectorize(math.erfc)
 
 
 @pytest.fixture(scope="module")
@@ -25,34 +21,8 @@ def F():
     return fp4q
 
 
-def phi64(x):
-    """Standard normal cdf as erfc(-x/sqrt 2)/2: no cancellation in the negative tail."""
-    return 0.5 * _erfc(-np.asarray(x, dtype=np.float64) / math.sqrt(2.0))
-
-
-def gelu64(x):
-    x = np.asarray(x, dtype=np.float64)
-    return x * phi64(x)
-
-
-def gelu_grad64(x):
-    x = np.asarray(x, dtype=np.float64)
-    return phi64(x) + x * np.exp(-0.5 * x * x) / math.sqrt(2.0 * math.pi)
-
-
 def u16(t):
     return t.cpu().view(torch.int16).numpy().view(np.uint16)
-
-
-def assert_bf16_near(got_u16, want64, ulps, what):
-    """bf16 results within `ulps` bf16 ulps of a float64 value (the epilogue's erff/expf are
-    not correctly rounded, so the last bf16 bit may differ)."""
-    got = bf16_values(got_u16).astype(np.float64)
-    want = np.asarray(want64, dtype=np.float64)
-    tol = ulps * np.maximum(np.abs(want), 2.0 ** -126) * 2.0 ** -7 + 2.0 ** -133
-    bad = np.abs(got - want) > tol
-    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} beyond {ulps} bf16 ulp; first "
-                           f"got {got[bad][0]!r} want {want[bad][0]!r}")
 
 
 @pytest.mark.parametrize("M,N,K", [(300, 272, 4096), (96, 256, 512), (512, 512, 1024)])
