@@ -76,9 +76,22 @@ __device__ __forceinline__ void global_scales(float amax, float& s_enc, float& s
     s_dec = __fdiv_rn(1.0f, s_enc);
 }
 
-// Block scale code and the local encode scale (steps 2-3).
+// amax_b / 6 correctly rounded, for amax_b a non-negative bf16 value: q0 = amax_b * RN(1/6), then
+// one fused multiply-add correction, q0 + RN(amax_b - 6 q0) * RN(1/6) (division by a constant
+// with a correction step, Brisebarre, Muller and Raina, "Accelerating correctly rounded
+// floating-point division when the divisor is known in advance", IEEE TC 2004). Equal to the
+// IEEE quotient for every one of the 32640 non-negative finite bf16 values (checked exhaustively
+// in exact arithmetic by the CPU tests).
+__device__ __forceinline__ float div6_bf16(float a) {
+    const float c = 0.16666667163372039795f;   // RN(1/6) = 0x3E2AAAAB
+    const float q0 = __fmul_rn(a, c);
+    const float r = __fmaf_rn(-q0, 6.0f, a);
+    return __fmaf_rn(r, c, q0);
+}
+
+// Block scale code and the local encode scale (steps 2-3); amax_b is a bf16 value.
 __device__ __forceinline__ uint32_t block_scale(float amax_b, float s_enc) {
-    float v = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc);
+    float v = __fmul_rn(div6_bf16(amax_b), s_enc);
     uint32_t sb = e4m3_rne_sat(v) & 0x7Fu;
     return sb == 0 ? 1u : sb;
 }
@@ -211,6 +224,11 @@ __global__ void __launch_bounds__(256) quantize_2d_kernel(const uint16_t* __rest
 // ---------------------------------------------------------------------------------------
 constexpr int kRowHoldMax = 4;
 
+// The low bytes of a, b, c, d as one word (a lowest): three byte permutes.
+__device__ __forceinline__ uint32_t pack_bytes4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
+}
+
 // Two fp32 values (a packed pair) -> their E2M1 codes (one byte, low nibble = low half, round
 // to nearest even, saturating) and the grid values of those codes as a packed fp32 pair.
 __device__ __forceinline__ uint32_t e2m1x2_roundtrip(uint64_t y2, uint64_t& q2) {
@@ -240,40 +258,34 @@ __device__ __forceinline__ void encode16_46(const uint32_t (&w)[8], float se6, f
     asm("mov.b64 %0, {%1, %1};" : "=l"(s4) : "f"(se4));
     asm("mov.b64 %0, {%1, %1};" : "=l"(a6) : "f"(0.0f));
     a4 = a6;
-    uint32_t lo6 = 0, hi6 = 0, lo4 = 0, hi4 = 0;
+    uint32_t b6[8], b4[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         uint64_t x2, y6, y4, q6, q4, d6, d4;
         asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "r"(w[j] << 16), "r"(w[j] & 0xFFFF0000u));
         asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y6) : "l"(x2), "l"(s6));
         asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y4) : "l"(x2), "l"(s4));
-        const uint32_t b6 = e2m1x2_roundtrip(y6, q6), b4 = e2m1x2_roundtrip(y4, q4);
+        b6[j] = e2m1x2_roundtrip(y6, q6);
+        b4[j] = e2m1x2_roundtrip(y4, q4);
         asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d6) : "l"(y6), "l"(q6));
         asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d4) : "l"(y4), "l"(q4));
         asm("fma.rn.f32x2 %0, %1, %1, %0;" : "+l"(a6) : "l"(d6));
         asm("fma.rn.f32x2 %0, %1, %1, %0;" : "+l"(a4) : "l"(d4));
-        if (j < 4) {
-            lo6 |= b6 << (8 * j);
-            lo4 |= b4 << (8 * j);
-        } else {
-            hi6 |= b6 << (8 * (j - 4));
-            hi4 |= b4 << (8 * (j - 4));
-        }
     }
     float e0, e1;
     asm("mov.b64 {%0, %1}, %2;" : "=f"(e0), "=f"(e1) : "l"(a6));
     sq6 = __fadd_rn(e0, e1);
     asm("mov.b64 {%0, %1}, %2;" : "=f"(e0), "=f"(e1) : "l"(a4));
     sq4 = __fadd_rn(e0, e1);
-    c6 = make_uint2(lo6, hi6);
-    c4 = make_uint2(lo4, hi4);
+    c6 = make_uint2(pack_bytes4(b6[0], b6[1], b6[2], b6[3]), pack_bytes4(b6[4], b6[5], b6[6], b6[7]));
+    c4 = make_uint2(pack_bytes4(b4[0], b4[1], b4[2], b4[3]), pack_bytes4(b4[4], b4[5], b4[6], b4[7]));
 }
 
 // Both candidate block scales from one hardware conversion (round to nearest even, saturating
 // at 448: the rule of e4m3_rne_sat): byte 0 for target 6, (amax_b / 6) * s_enc, and byte 1 for
 // target 4, (amax_b / 4) * s_enc; a scale that rounds to zero is raised to the smallest code.
 __device__ __forceinline__ uint32_t scale_codes_46(float amax_b, float s_enc) {
-    const float v6 = __fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc);
+    const float v6 = __fmul_rn(div6_bf16(amax_b), s_enc);
     const float v4 = __fmul_rn(__fmul_rn(amax_b, 0.25f), s_enc);     // amax_b / 4 is exact
     uint32_t c;
     asm("{.reg .b16 t; cvt.rn.satfinite.e4m3x2.f32 t, %1, %2; cvt.u32.u16 %0, t;}" : "=r"(c) : "f"(v4), "f"(v6));
