@@ -7,6 +7,8 @@ GELU(H), 16x16 quantize of W1 and W2, two NVFP4 GEMMs forward (GELU and max|GELU
 first one's epilogue); four MXFP8 requants with stochastic rounding (two with the 16-point
 RHT) and two MXFP8 GEMMs per layer backward (GELU' in the second layer's dgrad epilogue).
 The metric is the step's dense GEMM throughput (6 x 2 M D F FLOPs per step) in TFLOP/s.
+The line also reports the same step with the activations quantized per token row with
+Four Over Six block scales ("per_token_4over6"), timed separately.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -47,6 +49,8 @@ BYTES_PER_ELEM = {
     "requant_bf16": 2.0 + 1 + 1 / 32,
     "requant_nvfp4_1d": 0.5 + 1 / 16 + 1 + 1 / 32,
     "requant_nvfp4_2d": 0.5 + 1 / 256 + 1 + 1 / 32,
+    # per-token form: one pass, no amax kernel (the 4-byte row scale is left out: < 0.1%)
+    "quantize_1d_rows46": 2.0 + 0.5 + 1 / 16,
 }
 
 
@@ -178,26 +182,37 @@ class EventLog:
         return agg
 
 
-def mlp_step(F, torch, ins, log, seed, signs):
-    """One forward + backward of the MLP block, every call logged by kind."""
+def mlp_step(F, torch, ins, log, seed, signs, outer="tensor"):
+    """One forward + backward of the MLP block, every call logged by kind. outer="row": the
+    activations (X and GELU(H)) take one outer scale per token row and 4/6 block scales."""
     x, w1, w2, dy = ins
     M, D, Fh = M_TOK, D_MODEL, F_FFN
     L = log.wrap
+    rows = outer == "row"
+    x_kind = F.IN_NVFP4_1D_ROWS if rows else F.IN_NVFP4_1D
     # ---- forward
-    xc, xs, xsd, _ = L("quantize_1d", M * D, F.quantize_1d, x)
+    if rows:
+        xc, xs, xsd = L("quantize_1d_rows46", M * D, F.quantize_1d_rows, x, True)
+    else:
+        xc, xs, xsd, _ = L("quantize_1d", M * D, F.quantize_1d, x)
     w1c, w1s, w1d, _ = L("quantize_2d", Fh * D, F.quantize_2d, w1)
     # layer 1 with GELU in its epilogue: h, a = GELU(h) and max|a| (layer 2's quantize amax)
-    h, a, a_amax = L("gemm_nvfp4", 2.0 * M * Fh * D, F.gemm_nvfp4_gelu, xc, xs, xsd, w1c, w1s, F.SCALE_2D, w1d)
-    ac, as_, ad, _ = L("quantize_1d_given_amax", M * Fh, F.quantize_1d, a, amax_in=a_amax)
+    if rows:
+        h, a = L("gemm_nvfp4", 2.0 * M * Fh * D, F.gemm_nvfp4_gelu_rows, xc, xs, xsd, w1c, w1s, F.SCALE_2D, w1d)
+        ac, as_, ad = L("quantize_1d_rows46", M * Fh, F.quantize_1d_rows, a, True)
+    else:
+        h, a, a_amax = L("gemm_nvfp4", 2.0 * M * Fh * D, F.gemm_nvfp4_gelu, xc, xs, xsd, w1c, w1s, F.SCALE_2D, w1d)
+        ac, as_, ad, _ = L("quantize_1d_given_amax", M * Fh, F.quantize_1d, a, amax_in=a_amax)
     w2c, w2s, w2d, _ = L("quantize_2d", D * Fh, F.quantize_2d, w2)
-    y = L("gemm_nvfp4", 2.0 * M * D * Fh, F.gemm_nvfp4, ac, as_, ad, w2c, w2s, F.SCALE_2D, w2d, torch.bfloat16)
+    gemm2 = F.gemm_nvfp4_rows if rows else F.gemm_nvfp4
+    y = L("gemm_nvfp4", 2.0 * M * D * Fh, gemm2, ac, as_, ad, w2c, w2s, F.SCALE_2D, w2d, torch.bfloat16)
     # ---- backward, layer 2: dA = dY W2, dW2 = dY^T A_q
     g = L("requant_bf16", M * D, F.requant_mxfp8, F.IN_BF16, dy, None, None, M, D, 0, 0, 0, F.SR, seed, F.TAG_DY_ROWS)
     w2t = L("requant_nvfp4_2d", D * Fh, F.requant_mxfp8, F.IN_NVFP4_2D, w2c, w2s, w2d, D, Fh, 1, 0, 0, F.SR, seed, F.TAG_WT)
     # layer 2's dgrad with GELU' in its epilogue: dh = (dY W2) * GELU'(h)
     dh = L("gemm_mxfp8", 2.0 * M * Fh * D, F.gemm_mxfp8_dgelu, g[0], g[1], w2t[0], w2t[1], h)
     gt = L("requant_bf16", M * D, F.requant_mxfp8, F.IN_BF16, dy, None, None, M, D, 1, 1, signs, F.SR, seed, F.TAG_DY_T)
-    at = L("requant_nvfp4_1d", M * Fh, F.requant_mxfp8, F.IN_NVFP4_1D, ac, as_, ad, M, Fh, 1, 1, signs, F.SR, seed, F.TAG_XT)
+    at = L("requant_nvfp4_1d", M * Fh, F.requant_mxfp8, x_kind, ac, as_, ad, M, Fh, 1, 1, signs, F.SR, seed, F.TAG_XT)
     dw2 = L("gemm_mxfp8", 2.0 * D * Fh * M, F.gemm_mxfp8, gt[0], gt[1], at[0], at[1], torch.float32)
     # ---- backward, layer 1: dX = dH W1, dW1 = dH^T X_q  (own counter stream: seed2)
     seed2 = seed ^ 0x9E3779B97F4A7C15
@@ -205,7 +220,7 @@ def mlp_step(F, torch, ins, log, seed, signs):
     w1t = L("requant_nvfp4_2d", Fh * D, F.requant_mxfp8, F.IN_NVFP4_2D, w1c, w1s, w1d, Fh, D, 1, 0, 0, F.SR, seed2, F.TAG_WT)
     dx = L("gemm_mxfp8", 2.0 * M * D * Fh, F.gemm_mxfp8, g1[0], g1[1], w1t[0], w1t[1], torch.bfloat16)
     g1t = L("requant_bf16", M * Fh, F.requant_mxfp8, F.IN_BF16, dh, None, None, M, Fh, 1, 1, signs, F.SR, seed2, F.TAG_DY_T)
-    xt = L("requant_nvfp4_1d", M * D, F.requant_mxfp8, F.IN_NVFP4_1D, xc, xs, xsd, M, D, 1, 1, signs, F.SR, seed2, F.TAG_XT)
+    xt = L("requant_nvfp4_1d", M * D, F.requant_mxfp8, x_kind, xc, xs, xsd, M, D, 1, 1, signs, F.SR, seed2, F.TAG_XT)
     dw1 = L("gemm_mxfp8", 2.0 * Fh * D * M, F.gemm_mxfp8, g1t[0], g1t[1], xt[0], xt[1], torch.float32)
     return y, dx, dw1, dw2
 
@@ -213,7 +228,31 @@ def mlp_step(F, torch, ins, log, seed, signs):
 LAUNCHES_PER_STEP = {
     "amax": 3, "quantize_1d": 2, "quantize_2d": 2, "gemm_nvfp4": 2, "requant": 8, "gemm_mxfp8": 4,
 }
+# per-token form: the weights' two amax passes, no activation amax
+LAUNCHES_PER_STEP_ROWS = {
+    "amax": 2, "quantize_1d_rows": 2, "quantize_2d": 2, "gemm_nvfp4": 2, "requant": 8, "gemm_mxfp8": 4,
+}
 STEP_FLOPS = 6 * 2.0 * M_TOK * D_MODEL * F_FFN
+
+
+def summarize_kernels(kinds, peaks):
+    """Per call kind: launches, average duration and achieved rate against its roofline."""
+    kernels = {}
+    for kind, (n, tot_ms, units) in sorted(kinds.items()):
+        avg = tot_ms / n
+        if kind.startswith("gemm"):
+            tf = units / (tot_ms * 1e-3) / 1e12
+            peak = peaks["bf16_tflops_sustained"] * (RATIO_FP4 if kind == "gemm_nvfp4" else RATIO_FP8)
+            kernels[kind] = {"launches": n, "avg_ms": round(avg, 4), "achieved": round(tf, 1),
+                             "unit": "TFLOP/s", "peak": round(peak, 1), "frac": round(tf / peak, 4)}
+        else:
+            gbs = units * BYTES_PER_ELEM[kind] / (tot_ms * 1e-3) / 1e9
+            two_pass = kind in ("quantize_1d", "quantize_2d")
+            kernels[kind] = {"launches": n, "avg_ms": round(avg, 4), "achieved": round(gbs, 1),
+                             "unit": "GB/s (amax + quantize passes)" if two_pass else "GB/s",
+                             "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4)}
+        kernels[kind]["traffic"] = ncu_traffic(kind)      # DRAM bytes per launch (ncu), or None
+    return kernels
 
 
 def max_over_ranks(values, device):
@@ -339,29 +378,38 @@ def run_ours(args, rank, world, local_rank):
     if st != F.OK:
         raise RuntimeError("device status after timing: " + F.status_str(st))
 
+    # ---- the same step with per-token activation scales and 4/6 block scales
+    # (4bit.vizuara.ai §10), timed on its own after warm-up
+    rlog = EventLog(torch)
+    for _ in range(3):
+        mlp_step(F, torch, ins, rlog, seed, signs, outer="row")
+    r_steps = max(2, args.steps // 4)
+    barrier()
+    torch.cuda.synchronize()
+    rlog.on = True
+    r0 = torch.cuda.Event(enable_timing=True)
+    r1 = torch.cuda.Event(enable_timing=True)
+    r0.record()
+    for _ in range(r_steps):
+        mlp_step(F, torch, ins, rlog, seed, signs, outer="row")
+    r1.record()
+    torch.cuda.synchronize()
+    barrier()
+    rlog.on = False
+    r_ms = r0.elapsed_time(r1) / r_steps
+    st = F.fp4q_device_status()
+    if st != F.OK:
+        raise RuntimeError("device status after the per-token step: " + F.status_str(st))
+
     # ---- max over ranks
-    per_step, e2e_ms = max_over_ranks([ms / args.steps, e2e_ms], dev)
+    per_step, e2e_ms, r_ms = max_over_ranks([ms / args.steps, e2e_ms, r_ms], dev)
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return None
 
     peaks, peak_src = load_peaks()
-    kernels = {}
-    for kind, (n, tot_ms, units) in sorted(kinds.items()):
-        avg = tot_ms / n
-        if kind.startswith("gemm"):
-            tf = units / (tot_ms * 1e-3) / 1e12
-            peak = peaks["bf16_tflops_sustained"] * (RATIO_FP4 if kind == "gemm_nvfp4" else RATIO_FP8)
-            kernels[kind] = {"launches": n, "avg_ms": round(avg, 4), "achieved": round(tf, 1),
-                             "unit": "TFLOP/s", "peak": round(peak, 1), "frac": round(tf / peak, 4)}
-        else:
-            gbs = units * BYTES_PER_ELEM[kind] / (tot_ms * 1e-3) / 1e9
-            kernels[kind] = {"launches": n, "avg_ms": round(avg, 4), "achieved": round(gbs, 1),
-                             "unit": "GB/s (amax + quantize passes)" if kind.startswith("quantize") else "GB/s",
-                             "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4)}
-    for kind in kernels:
-        kernels[kind]["traffic"] = ncu_traffic(kind)      # DRAM bytes per launch (ncu), or None
+    kernels = summarize_kernels(kinds, peaks)
     dom = max(kinds.items(), key=lambda kv: kv[1][1])[0]
     n, tot_ms, units = kinds[dom]
     traffic = ncu_traffic(dom)
@@ -390,6 +438,15 @@ def run_ours(args, rank, world, local_rank):
                 "wall_ms": round(e2e_wall_ms, 3)},
         "gpu_launches": int(sum(LAUNCHES_PER_STEP.values()) * args.steps),
         "clocks": clocks,
+        "per_token_4over6": {
+            "what": "the same step with the activations quantized per token row with 4/6 block scales "
+                    "(one pass, no activation amax), per-row outer scales through both GEMM epilogues "
+                    "and the X^T requantizations",
+            "value": round(STEP_FLOPS / (r_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(r_ms, 4), "steps": r_steps, "warmup": 3,
+            "gpu_launches": int(sum(LAUNCHES_PER_STEP_ROWS.values()) * r_steps),
+            "kernels": summarize_kernels(rlog.totals(), peaks),
+        },
     }
     if world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.cpu_sample)
