@@ -574,3 +574,119 @@ EXPORT void orc_requant_mxfp8(int in_kind, const void* in, const uint8_t* in_sca
     orc_requant_mxfp8_rows(in_kind, in, in_scales, s_dec, s_dec_rows, rows, cols, transpose, rht, rht_signs,
                            rounding, seed, tag, 0, transpose ? cols : rows, out_e4m3, out_e8m0);
 }
+
+/* ------------------------------------------------------------------------- */
+/* The MoE combine wire format: RHT32 + block-scaled S2F6.                    */
+/* [VZ] §11: rotate 32 values at a time (flip signs by a fixed random         */
+/* pattern, then 32 sums and differences of all of them, each divided by      */
+/* sqrt(32)); quantize to S2F6, an 8-bit signed integer divided by 64         */
+/* (-2 .. 127/64 in steps of 1/64), with one power-of-two scale per 32         */
+/* values (8.25 bits per value); the receiver dequantizes and adds up the      */
+/* arrivals, then undoes the rotation. [TML] "合并阶段": RHT32, then blocked    */
+/* S2F6 with an E8M0 scale per 32; dequantize and aggregate on arrival, then  */
+/* inverse Hadamard.                                                          */
+/* Readings where the pages are silent:                                       */
+/*   - the rotation is y = c * H32 (s o x) with c = RN(1/sqrt(32)) in fp32:   */
+/*     signs first, butterflies at distances 1, 2, 4, 8, 16, then one         */
+/*     multiply by c per value; its inverse applies the same butterflies and  */
+/*     c, then the signs (H32 is symmetric and (H32/sqrt 32)^2 = I);          */
+/*   - the block exponent is the ceiling rule of the MXFP8 path with the      */
+/*     S2F6 maximum 127/64: the smallest e with amax <= (127/64) 2^e, clamped */
+/*     to [-127, 127], E8M0 byte e + 127; nothing saturates below the clamp;  */
+/*   - q = round-half-even(y * 2^(6 - e)), clamped to [-128, 127], stored as  */
+/*     a two's-complement byte; value q * 2^(e - 6);                          */
+/*   - arrivals are summed in fp32 in index order (slot 0 first), in the      */
+/*     rotated domain, and the sum is rotated back once (the rotation is      */
+/*     linear).                                                               */
+/* ------------------------------------------------------------------------- */
+static const float kRhtC32 = 0.17677669529663688f;   /* RN(1/sqrt(32)) */
+
+static void fwht32(float* v)
+{
+    for (int h = 1; h < 32; h <<= 1)
+        for (int i = 0; i < 32; ++i)
+            if ((i & h) == 0) {
+                float a = v[i], b = v[i + h];
+                v[i] = a + b;
+                v[i + h] = a - b;
+            }
+}
+
+/* Forward rotation of one group of 32, in place. */
+EXPORT void orc_rht32_group(float* v, uint32_t signs)
+{
+    for (int i = 0; i < 32; ++i)
+        if ((signs >> i) & 1u) v[i] = -v[i];
+    fwht32(v);
+    for (int i = 0; i < 32; ++i) v[i] = v[i] * kRhtC32;
+}
+
+/* Inverse rotation of one group of 32, in place. */
+EXPORT void orc_irht32_group(float* v, uint32_t signs)
+{
+    fwht32(v);
+    for (int i = 0; i < 32; ++i) v[i] = v[i] * kRhtC32;
+    for (int i = 0; i < 32; ++i)
+        if ((signs >> i) & 1u) v[i] = -v[i];
+}
+
+/* S2F6 block quantize of 32 fp32 values: codes (two's-complement bytes) and the
+ * E8M0 byte. */
+EXPORT void orc_s2f6_block(const float* y, uint8_t* codes, uint8_t* e8m0)
+{
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) if (fabs((double)y[i]) > amax) amax = fabs((double)y[i]);
+    int e = orc_pow2_ceil_exponent(amax, 127.0 / 64.0);
+    *e8m0 = (uint8_t)(e + 127);
+    for (int i = 0; i < 32; ++i) {
+        double t = ldexp((double)y[i], 6 - e);           /* exact */
+        double q = nearbyint(t);                         /* ties to even (default mode) */
+        if (q > 127.0) q = 127.0;
+        if (q < -128.0) q = -128.0;
+        codes[i] = (uint8_t)(int8_t)q;
+    }
+}
+
+EXPORT double orc_s2f6_decode(uint8_t code, uint8_t e8m0)
+{
+    return ldexp((double)(int8_t)code, (int)e8m0 - 127 - 6);
+}
+
+/* Encode a [rows][cols] tensor (fp32, or bf16 when in_is_bf16), groups of 32 along
+ * the rows: RHT32 then S2F6. codes [rows][cols], e8m0 [rows][cols/32]. */
+EXPORT void orc_combine_encode(const void* in, int in_is_bf16, int64_t rows, int64_t cols,
+                               uint32_t signs, uint8_t* codes, uint8_t* e8m0)
+{
+    float v[32];
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t g = 0; g < cols / 32; ++g) {
+            for (int i = 0; i < 32; ++i) {
+                int64_t k = r * cols + g * 32 + i;
+                v[i] = in_is_bf16 ? bf16_value(((const uint16_t*)in)[k]) : ((const float*)in)[k];
+            }
+            orc_rht32_group(v, signs);
+            orc_s2f6_block(v, &codes[r * cols + g * 32], &e8m0[r * (cols / 32) + g]);
+        }
+}
+
+/* Decode: token t's k arrivals are rows t*k .. t*k+k-1 of codes / e8m0; their
+ * dequantized values are summed in fp32 (slot order), then rotated back.
+ * out [tokens][cols] fp32. */
+EXPORT void orc_combine_decode(const uint8_t* codes, const uint8_t* e8m0, int64_t tokens, int64_t k,
+                               int64_t cols, uint32_t signs, float* out)
+{
+    float acc[32];
+    for (int64_t t = 0; t < tokens; ++t)
+        for (int64_t g = 0; g < cols / 32; ++g) {
+            for (int64_t j = 0; j < k; ++j) {
+                int64_t r = t * k + j;
+                uint8_t sc = e8m0[r * (cols / 32) + g];
+                for (int i = 0; i < 32; ++i) {
+                    float z = (float)orc_s2f6_decode(codes[r * cols + g * 32 + i], sc);   /* exact */
+                    acc[i] = (j == 0) ? z : acc[i] + z;
+                }
+            }
+            orc_irht32_group(acc, signs);
+            for (int i = 0; i < 32; ++i) out[t * cols + g * 32 + i] = acc[i];
+        }
+}

@@ -94,6 +94,18 @@ def lib():
         L.orc_requant_mxfp8.argtypes = [ctypes.c_int, ctypes.c_void_p, _u8p, ctypes.c_float,
                                         _f32p, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
                                         ctypes.c_int, ctypes.c_uint64, ctypes.c_uint32, _u8p, _u8p]
+        L.orc_rht32_group.restype = None
+        L.orc_rht32_group.argtypes = [_f32p, ctypes.c_uint32]
+        L.orc_irht32_group.restype = None
+        L.orc_irht32_group.argtypes = [_f32p, ctypes.c_uint32]
+        L.orc_s2f6_block.restype = None
+        L.orc_s2f6_block.argtypes = [_f32p, _u8p, _u8p]
+        L.orc_s2f6_decode.restype = ctypes.c_double
+        L.orc_s2f6_decode.argtypes = [ctypes.c_uint8, ctypes.c_uint8]
+        L.orc_combine_encode.restype = None
+        L.orc_combine_encode.argtypes = [ctypes.c_void_p, ctypes.c_int, _i64, _i64, ctypes.c_uint32, _u8p, _u8p]
+        L.orc_combine_decode.restype = None
+        L.orc_combine_decode.argtypes = [_u8p, _u8p, _i64, _i64, _i64, ctypes.c_uint32, _f32p]
         _LIB = L
     return _LIB
 
@@ -304,6 +316,57 @@ def requant_mxfp8(in_kind, data, scales, s_dec, rows, cols, transpose, rht, rht_
                                  int(bool(transpose)), int(bool(rht)), int(rht_signs), rounding,
                                  int(seed), int(tag), b, e, _p(e4, _u8p), _p(e8, _u8p))
     return e4, e8
+
+
+# ---------------------------------------------------------------- combine codec (RHT32 + S2F6)
+def rht32_group(v, signs):
+    v = _c(v, np.float32).copy()
+    assert v.size == 32
+    lib().orc_rht32_group(_p(v, _f32p), int(signs))
+    return v
+
+
+def irht32_group(v, signs):
+    v = _c(v, np.float32).copy()
+    assert v.size == 32
+    lib().orc_irht32_group(_p(v, _f32p), int(signs))
+    return v
+
+
+def s2f6_block(y):
+    """32 fp32 values -> (codes uint8[32] two's complement, e8m0 byte)."""
+    y = _c(y, np.float32)
+    codes = np.zeros(32, np.uint8)
+    e8 = np.zeros(1, np.uint8)
+    lib().orc_s2f6_block(_p(y, _f32p), _p(codes, _u8p), _p(e8, _u8p))
+    return codes, int(e8[0])
+
+
+def s2f6_decode(code, e8m0):
+    return lib().orc_s2f6_decode(int(code) & 0xFF, int(e8m0))
+
+
+def combine_encode(x, signs, is_bf16=False):
+    """[rows, cols] fp32 (or bf16 bits) -> (codes uint8 [rows, cols], e8m0 uint8 [rows, cols/32])."""
+    x = _c(x, np.uint16 if is_bf16 else np.float32)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols), np.uint8)
+    e8 = np.zeros((rows, cols // 32), np.uint8)
+    lib().orc_combine_encode(x.ctypes.data, int(bool(is_bf16)), rows, cols, int(signs),
+                             _p(codes, _u8p), _p(e8, _u8p))
+    return codes, e8
+
+
+def combine_decode(codes, e8m0, k, signs):
+    """codes [tokens*k, cols], e8m0 [tokens*k, cols/32] -> fp32 [tokens, cols]: the k arrivals
+    of each token summed, then rotated back."""
+    codes = _c(codes, np.uint8)
+    e8m0 = _c(e8m0, np.uint8)
+    rows, cols = codes.shape
+    assert rows % k == 0
+    out = np.zeros((rows // k, cols), np.float32)
+    lib().orc_combine_decode(_p(codes, _u8p), _p(e8m0, _u8p), rows // k, k, cols, int(signs), _p(out, _f32p))
+    return out
 
 
 # ---------------------------------------------------------------- GEMMs

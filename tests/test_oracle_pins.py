@@ -708,3 +708,131 @@ def test_gemm_nvfp4_rows_brute_force(orc):
                 vb = orc.e2m1_decode(code(bc, n, k)) * orc.e4m3_decode(bsc[n // 16, k // 16]) * sb
                 acc += va * vb
             assert abs(D[m, n] - acc) <= 1e-12 * max(1.0, abs(acc))
+
+
+# ------------------------------------------------------------------ combine codec: RHT32 + S2F6
+def test_s2f6_grid_matches_page(orc, worked):
+    ex = worked["s2f6"]
+    vals = sorted(orc.s2f6_decode(c, 127) for c in range(256))        # E8M0 127: scale 1
+    assert vals[0] == ex["lo"] and vals[-1] == ex["hi"]
+    assert np.allclose(np.diff(vals), ex["step"], rtol=0, atol=0)
+    assert (8 * 32 + 8) / 32 == ex["bits"]
+    # the scale is a plain power of two
+    assert orc.s2f6_decode(64, 130) == 8.0 and orc.s2f6_decode(0x80, 120) == -2.0 * 2.0 ** -7
+
+
+def test_rht32_is_the_normalised_sylvester_hadamard(orc):
+    c = float(np.float32(0.17677669529663688))             # RN(1/sqrt(32))
+    for signs in (0, 0x8000_0001, 0x5A5A_C3C3):
+        cols = []
+        for j in range(32):
+            e = np.zeros(32, np.float32)
+            e[j] = 1.0
+            cols.append(orc.rht32_group(e, signs))
+        H = np.array(cols).T
+        i = np.arange(32)
+        want = np.array([[(-1) ** bin(a & b).count("1") for b in i] for a in i], np.float64)
+        s = np.array([-1.0 if (signs >> k) & 1 else 1.0 for k in range(32)])
+        assert np.array_equal(H, (want * s[None, :] * c).astype(np.float32))
+        assert np.allclose(H @ H.T, np.eye(32), atol=1e-6)
+
+
+def test_rht32_inverse_energy_and_outlier_spread(orc, worked):
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(32).astype(np.float32)
+    signs = 0x1234_ABCD
+    y = orc.rht32_group(x, signs)
+    assert abs(np.linalg.norm(y) / np.linalg.norm(x) - 1) < 1e-6
+    assert np.allclose(orc.irht32_group(y, signs), x, rtol=0, atol=1e-6)
+    spike = np.zeros(32, np.float32)
+    spike[7] = worked["rht_outlier"]["x"]
+    out = orc.rht32_group(spike, signs)
+    assert np.allclose(np.abs(out), worked["rht_outlier"]["each32"], atol=0.01)
+
+
+def test_s2f6_scale_rule_rounding_and_saturation(orc):
+    # the block max decides: amax <= (127/64) 2^e for the smallest e
+    for k in (-3, 0, 5):
+        y = np.zeros(32, np.float32)
+        y[0] = 127 / 64 * 2.0 ** k
+        codes, e8 = orc.s2f6_block(y)
+        assert e8 == 127 + k and np.int8(codes[0]) == 127
+        y[0] = np.nextafter(np.float32(y[0]), np.float32(np.inf))
+        codes, e8 = orc.s2f6_block(y)
+        assert e8 == 128 + k
+    zero_codes, zero_e8 = orc.s2f6_block(np.zeros(32, np.float32))
+    assert zero_e8 == 0 and not zero_codes.any()
+    # ties to even in units of 1/64 of the scale (block max 1.5 -> e = 0)
+    y = np.zeros(32, np.float32)
+    y[:6] = [1.5, 2.5 / 64, 3.5 / 64, -2.5 / 64, -0.5 / 64, 0.5 / 64]
+    codes, e8 = orc.s2f6_block(y)
+    assert e8 == 127
+    assert [int(np.int8(c)) for c in codes[:6]] == [96, 2, 4, -2, 0, 0]
+    # negative values use the full range down to -2 only when the positive side allows it
+    y[:] = -1.0
+    codes, e8 = orc.s2f6_block(y)
+    assert e8 == 127 and np.all(codes.view(np.int8) == -64)
+
+
+def test_combine_decode_sums_arrivals_then_rotates_back(orc):
+    rng = np.random.default_rng(4)
+    signs = 0x0F0F_3C3C
+    k, tokens, cols = 3, 5, 64
+    x = rng.standard_normal((tokens * k, cols)).astype(np.float32) * 3
+    codes, e8 = orc.combine_encode(x, signs)
+    out = orc.combine_decode(codes, e8, k, signs)
+    for t in range(tokens):
+        for g in range(cols // 32):
+            acc = None
+            for j in range(k):
+                r = t * k + j
+                z = np.array([orc.s2f6_decode(c, e8[r, g]) for c in codes[r, 32 * g:32 * g + 32]], np.float32)
+                acc = z if acc is None else (acc + z).astype(np.float32)
+            assert np.array_equal(out[t, 32 * g:32 * g + 32], orc.irht32_group(acc, signs))
+    # and it approximates the sum of the inputs
+    ref = x.reshape(tokens, k, cols).sum(axis=1)
+    assert np.linalg.norm(out - ref) / np.linalg.norm(ref) < 0.02
+
+
+def test_combine_round_trip_within_half_a_step(orc):
+    """One arrival: each value's rotated-domain error is at most half a step 2^(e-7); the
+    rotation back is orthonormal, so each group's error norm is at most sqrt(32) 2^(e-7)."""
+    x = inputs.student_t(16, 256, seed=5, df=3, scale=1.0).float().numpy()
+    signs = 0xDEAD_BEEF
+    codes, e8 = orc.combine_encode(x, signs)
+    out = orc.combine_decode(codes, e8, 1, signs)
+    err = np.linalg.norm((out - x).reshape(16, 8, 32), axis=2)
+    bound = np.sqrt(32) * 2.0 ** (e8.astype(np.float64) - 127 - 7)
+    assert np.all(err <= bound * (1 + 1e-5) + 1e-5 * np.linalg.norm(x.reshape(16, 8, 32), axis=2))
+
+
+def test_wire_format_errors_order_like_page(orc, worked):
+    """4bit.vizuara.ai §11 on real MLP outputs: MXFP8 2.66% > S2F6 0.92% > RHT32 + S2F6 0.79%, and
+    the rotation lowers the kurtosis (59 -> 7) and the spikiest block (5.6x -> 1.3x). The same
+    ordering holds on heavy-tailed synthetic outputs (Student-t, 3 degrees of freedom)."""
+    ex = worked["wire"]
+    x = inputs.student_t(64, 1024, seed=6, df=3, scale=1.0).float().numpy()
+    xb = np.ascontiguousarray(x.astype(np.float32))
+    n = np.linalg.norm(xb)
+    e4, e8 = orc.requant_mxfp8(orc.IN_BF16, inputs.bf16_bits(inputs.student_t(64, 1024, seed=6, df=3, scale=1.0)),
+                               None, 1.0, 64, 1024, False, False, 0, orc.RNE, 0, 1)
+    e_mx = np.linalg.norm(orc.dequant_mxfp8(e4, e8) - xb) / n
+    # S2F6 without the rotation: quantize the raw blocks
+    raw = np.zeros_like(xb)
+    for r in range(64):
+        for g in range(32):
+            cc, ee = orc.s2f6_block(xb[r, 32 * g:32 * g + 32])
+            raw[r, 32 * g:32 * g + 32] = [orc.s2f6_decode(q, ee) for q in cc]
+    e_s2f6 = np.linalg.norm(raw - xb) / n
+    signs = 0x9E37_79B9
+    c, s = orc.combine_encode(xb, signs)
+    e_rht = np.linalg.norm(orc.combine_decode(c, s, 1, signs) - xb) / n
+    assert e_mx > e_s2f6 > e_rht, (e_mx, e_s2f6, e_rht)
+    assert e_mx / e_s2f6 > 0.5 * ex["mxfp8"] / ex["s2f6"]
+    blocks = xb.reshape(-1, 32)
+    rot = np.array([orc.rht32_group(b, signs) for b in blocks])
+    kurt = lambda v: float(np.mean(v ** 4) / np.mean(v ** 2) ** 2)
+    assert kurt(rot) < kurt(blocks) / 2 and kurt(rot) < ex["kurt"]
+    spike = lambda b: float(np.max(np.abs(b)) / np.sqrt(np.mean(b ** 2)))
+    worst = int(np.argmax([spike(b) for b in blocks]))
+    assert spike(rot[worst]) < spike(blocks[worst]) / 2
