@@ -8,7 +8,8 @@ first one's epilogue); four MXFP8 requants with stochastic rounding (two with th
 RHT) and two MXFP8 GEMMs per layer backward (GELU' in the second layer's dgrad epilogue).
 The metric is the step's dense GEMM throughput (6 x 2 M D F FLOPs per step) in TFLOP/s.
 The line also reports the same step with the activations quantized per token row with
-Four Over Six block scales ("per_token_4over6"), timed separately.
+Four Over Six block scales ("per_token_4over6"), timed separately, and the MoE combine wire
+format (RHT32 + S2F6) at the MoE layer's size ("combine_codec").
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -51,6 +52,11 @@ BYTES_PER_ELEM = {
     "requant_nvfp4_2d": 0.5 + 1 / 256 + 1 + 1 / 32,
     # per-token form: one pass, no amax kernel (the 4-byte row scale is left out: < 0.1%)
     "quantize_1d_rows46": 2.0 + 0.5 + 1 / 16,
+    # combine wire format (RHT32 + S2F6, 8.25 bits per value)
+    "combine_encode_f32": 4.0 + 1 + 1 / 32,
+    "combine_encode_bf16": 2.0 + 1 + 1 / 32,
+    "combine_decode_k1_f32": 1 + 1 / 32 + 4.0,
+    "combine_decode_k2_bf16": 2 * (1 + 1 / 32) + 2.0,
 }
 
 
@@ -242,7 +248,7 @@ def summarize_kernels(kinds, peaks):
         avg = tot_ms / n
         if kind.startswith("gemm"):
             tf = units / (tot_ms * 1e-3) / 1e12
-            peak = peaks["bf16_tflops_sustained"] * (RATIO_FP4 if kind == "gemm_nvfp4" else RATIO_FP8)
+            peak = peaks["bf16_tflops_sustained"] * (RATIO_FP4 if kind.startswith("gemm_nvfp4") else RATIO_FP8)
             kernels[kind] = {"launches": n, "avg_ms": round(avg, 4), "achieved": round(tf, 1),
                              "unit": "TFLOP/s", "peak": round(peak, 1), "frac": round(tf / peak, 4)}
         else:
@@ -253,6 +259,51 @@ def summarize_kernels(kinds, peaks):
                              "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4)}
         kernels[kind]["traffic"] = ncu_traffic(kind)      # DRAM bytes per launch (ncu), or None
     return kernels
+
+
+def combine_section(F, torch, dev, peaks, iters=10):
+    """The MoE combine wire format (RHT32 + S2F6) at the MoE layer's size: the expert down
+    projection as a grouped NVFP4 GEMM with a bf16 output and with the encode in its epilogue,
+    the stand-alone encoder, and the receiver's decode (one and two arrivals per token)."""
+    from mxfp8_precision_numerics_gb300 import inputs as I
+    T, D, FE, E = 8192, 4096, 1536, 8          # tokens, d_model, expert ffn, experts (top-1, 1024 each)
+    signs = 0x9E3779B9
+    h = I.normal(T, FE, seed=31).to(dev)
+    w2 = I.normal(E * D, FE, seed=32, std=0.02).view(E, D, FE).to(dev)
+    hc, hs, hsd, _ = F.quantize_1d(h)
+    wc, ws, wsd, _ = F.quantize_2d(w2)
+    offs = [i * (T // E) for i in range(E + 1)]
+    y32 = I.student_t(T, D, seed=33, df=3, scale=1.0).float().to(dev)
+    y16 = y32.to(torch.bfloat16)
+    codes2, e82 = F.combine_encode(I.student_t(2 * T, D, seed=34, df=3, scale=1.0).float().to(dev), signs)
+    log = EventLog(torch)
+    L = log.wrap
+    flops = 2.0 * T * D * FE
+
+    def once():
+        L("gemm_nvfp4_grouped_bf16", flops, F.gemm_nvfp4, hc, hs, hsd, wc, ws, F.SCALE_2D, wsd, torch.bfloat16,
+          E, offs)
+        c, e8 = L("gemm_nvfp4_grouped_combine", flops, F.gemm_nvfp4_combine, hc, hs, hsd, wc, ws, F.SCALE_2D, wsd,
+                  signs, E, offs)
+        L("combine_encode_f32", T * D, F.combine_encode, y32, signs)
+        L("combine_encode_bf16", T * D, F.combine_encode, y16, signs)
+        L("combine_decode_k1_f32", T * D, F.combine_decode, c, e8, 1, signs, torch.float32)
+        L("combine_decode_k2_bf16", T * D, F.combine_decode, codes2, e82, 2, signs, torch.bfloat16)
+
+    for _ in range(3):
+        once()
+    torch.cuda.synchronize()
+    log.on = True
+    for _ in range(iters):
+        once()
+    torch.cuda.synchronize()
+    log.on = False
+    st = F.fp4q_device_status()
+    if st != F.OK:
+        raise RuntimeError("device status after the combine section: " + F.status_str(st))
+    return {"workload": f"MoE combine: {T} tokens x d_model {D}, {E} experts x {T // E} tokens (top-1), "
+                        f"expert ffn {FE}; decode k=2 on {2 * T} arrivals; inputs N(0,1) / Student-t(3)",
+            "iterations": iters, "kernels": summarize_kernels(log.totals(), peaks)}
 
 
 def max_over_ranks(values, device):
@@ -448,6 +499,7 @@ def run_ours(args, rank, world, local_rank):
             "kernels": summarize_kernels(rlog.totals(), peaks),
         },
     }
+    res["combine_codec"] = combine_section(F, torch, dev, peaks)
     if world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.cpu_sample)
     if dist is not None:

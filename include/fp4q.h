@@ -300,6 +300,53 @@ FP4Q_API int fp4q_gemm_mxfp8_dgelu(const uint8_t* a, const uint8_t* a_scales,
                     int64_t M, int64_t N, int64_t K, fp4q_stream_t stream);
 
 /*
+ * The MoE combine wire format: RHT32 + block-scaled S2F6 ([VZ] §11, "Combine is harder";
+ * [TML] 合并阶段). A layer output is rotated in groups of 32 consecutive values of a row and
+ * sent as S2F6 (8.25 bits per value); the receiver sums the dequantized arrivals of a token
+ * and rotates the sum back.
+ *   rotation  y = c * H32 (s o x): bit i of rht_signs set -> s_i = -1; Sylvester H32 evaluated
+ *             as butterflies at distances 1, 2, 4, 8, 16 in fp32; c = RN(1/sqrt 32) applied to
+ *             each value once. Inverse: butterflies, c, then the signs.
+ *   S2F6      e = the smallest integer with max|y| <= (127/64) 2^e over the group, clamped to
+ *             [-127, 127]; E8M0 byte e + 127; code q = round-half-even(y 2^(6-e)) clamped to
+ *             [-128, 127], stored as a two's-complement byte; value q 2^(e-6).
+ */
+
+/*
+ * fp4q_combine_encode — rotate and quantize a [rows][cols] tensor (groups of 32 along rows).
+ *   x          fp32 or bf16 (x_dtype FP4Q_F32 / FP4Q_BF16) [rows][cols], 16-byte aligned
+ *   codes      [rows][cols] S2F6 bytes, 16-byte aligned; e8m0 [rows][cols/32]
+ *   rows >= 1, cols % 32 == 0.
+ */
+FP4Q_API int fp4q_combine_encode(const void* x, int x_dtype, int64_t rows, int64_t cols, uint32_t rht_signs,
+                    uint8_t* codes, uint8_t* e8m0, fp4q_stream_t stream);
+
+/*
+ * fp4q_combine_decode — sum each token's k arrivals and rotate the sum back.
+ *   codes, e8m0  [tokens * k][cols] and [tokens * k][cols/32]: token t's arrivals are rows
+ *                t*k .. t*k+k-1, summed in fp32 in that order (exact dequantized values)
+ *   out          [tokens][cols] fp32 or bf16 (out_dtype; bf16 = round to nearest even of the
+ *                fp32 result), 16-byte aligned; codes 16-byte aligned
+ *   tokens >= 1, k >= 1, cols % 32 == 0.
+ */
+FP4Q_API int fp4q_combine_decode(const uint8_t* codes, const uint8_t* e8m0, int64_t tokens, int64_t k,
+                    int64_t cols, uint32_t rht_signs, void* out, int out_dtype, fp4q_stream_t stream);
+
+/*
+ * fp4q_gemm_nvfp4_combine — fp4q_gemm_nvfp4 (grouped or not) whose epilogue rotates each row's
+ * groups of 32 output values and writes them in the combine wire format instead of a float
+ * output ([VZ] §11: rotation and conversion at the very end of the GEMM kernel). The values
+ * encoded are the fp32 outputs fp4q_gemm_nvfp4 would store (accumulator x s_dec_a x s_dec_b).
+ *   codes_out  [M][N] S2F6 bytes, 16-byte aligned; e8m0_out [M][N/32]
+ *   N % 32 == 0; every other argument as fp4q_gemm_nvfp4.
+ */
+FP4Q_API int fp4q_gemm_nvfp4_combine(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec,
+                    const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
+                    const float* b_s_dec, uint32_t rht_signs, uint8_t* codes_out, uint8_t* e8m0_out,
+                    int64_t M, int64_t N, int64_t K,
+                    int groups, const int64_t* group_row_offsets_host, fp4q_stream_t stream);
+
+/*
  * fp4q_device_status — synchronizes `stream`, then reads and clears the library's device-side
  * error word. Returns FP4Q_ERR_TIMEOUT if a kernel's bounded wait (a GEMM pipeline barrier)
  * gave up since the last call, FP4Q_ERR_CUDA if the stream reports an error, else FP4Q_OK.

@@ -230,6 +230,62 @@ int fp4q_gemm_nvfp4_rows(const uint8_t* a, const uint8_t* a_scales, const float*
                            M, N, K, groups, group_row_offsets_host, stream);
 }
 
+int fp4q_gemm_nvfp4_combine(const uint8_t* a, const uint8_t* a_scales, const float* a_s_dec,
+                            const uint8_t* b, const uint8_t* b_scales, int b_scale_kind,
+                            const float* b_s_dec, uint32_t rht_signs, uint8_t* codes_out, uint8_t* e8m0_out,
+                            int64_t M, int64_t N, int64_t K,
+                            int groups, const int64_t* group_row_offsets_host, fp4q_stream_t stream) {
+    if (b_scale_kind != FP4Q_SCALE_1D && b_scale_kind != FP4Q_SCALE_2D) return FP4Q_ERR_ARG;
+    if (!a || !a_scales || !a_s_dec || !b || !b_scales || !b_s_dec || !codes_out || !e8m0_out) return FP4Q_ERR_NULL;
+    if (int v = validate_groups(groups, group_row_offsets_host, M)) return v;
+    if (M < 1 || N < 32 || N % 32 != 0 || K < 256 || K % 256 != 0) return FP4Q_ERR_SHAPE;
+    if (M > 2147483647 || N * groups > 2147483647) return FP4Q_ERR_SHAPE;
+    if (!al16(a) || !al16(b) || !al16(a_scales) || !al16(b_scales) || !al16(codes_out)) return FP4Q_ERR_ALIGN;
+    if (int dv = check_device()) return dv;
+    fp4q::GemmArgs g;
+    g.kind = 0;
+    g.a = a;
+    g.a_scales = a_scales;
+    g.a_s_dec = a_s_dec;
+    g.b = b;
+    g.b_scales = b_scales;
+    g.b_scale_kind = b_scale_kind;
+    g.b_s_dec = b_s_dec;
+    g.d = codes_out;
+    g.d_bf16 = 0;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.groups = groups;
+    g.group_offsets = group_row_offsets_host;
+    g.epi = 3;
+    g.d2 = e8m0_out;
+    g.rht32_signs = rht_signs;
+    return cuda_status(fp4q::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp4q_combine_encode(const void* x, int x_dtype, int64_t rows, int64_t cols, uint32_t rht_signs,
+                        uint8_t* codes, uint8_t* e8m0, fp4q_stream_t stream) {
+    if (x_dtype != FP4Q_F32 && x_dtype != FP4Q_BF16) return FP4Q_ERR_ARG;
+    if (!x || !codes || !e8m0) return FP4Q_ERR_NULL;
+    if (rows < 1 || cols < 32 || cols % 32 != 0) return FP4Q_ERR_SHAPE;
+    if (!al16(x) || !al16(codes)) return FP4Q_ERR_ALIGN;
+    if (int d = check_device()) return d;
+    return cuda_status(fp4q::launch_combine_encode(x, x_dtype == FP4Q_BF16, rows, cols, rht_signs, codes, e8m0,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp4q_combine_decode(const uint8_t* codes, const uint8_t* e8m0, int64_t tokens, int64_t k, int64_t cols,
+                        uint32_t rht_signs, void* out, int out_dtype, fp4q_stream_t stream) {
+    if (out_dtype != FP4Q_F32 && out_dtype != FP4Q_BF16) return FP4Q_ERR_ARG;
+    if (!codes || !e8m0 || !out) return FP4Q_ERR_NULL;
+    if (tokens < 1 || k < 1 || cols < 32 || cols % 32 != 0) return FP4Q_ERR_SHAPE;
+    if (!al16(codes) || !al16(out)) return FP4Q_ERR_ALIGN;
+    if (int d = check_device()) return d;
+    return cuda_status(fp4q::launch_combine_decode(codes, e8m0, tokens, k, cols, rht_signs, out,
+                                                   out_dtype == FP4Q_BF16, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fp4q_gemm_mxfp8(const uint8_t* a, const uint8_t* a_scales,
                     const uint8_t* b, const uint8_t* b_scales,
                     void* d, int d_dtype, int64_t M, int64_t N, int64_t K,

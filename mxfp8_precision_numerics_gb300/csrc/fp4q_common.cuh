@@ -269,4 +269,82 @@ __device__ __forceinline__ void rht16_inplace(float* v, uint32_t signs) {
     fwht16_quarter(v);
 }
 
+// ---------------------------------------------------------------------------------------
+// The combine wire format (4bit.vizuara.ai §11; "End-to-End 4-Bit Training" (Thinking
+// Machines), 合并阶段): rotate groups of 32 values (sign flips, Sylvester H32 butterflies at
+// distances 1, 2, 4, 8, 16 in fp32, then one multiply by RN(1/sqrt 32)), then S2F6 (a signed
+// 8-bit integer over 64) with one E8M0 scale per 32: e = the smallest integer with
+// amax <= (127/64) 2^e, clamped to [-127, 127]; q = round-half-even(y 2^(6-e)) in [-128, 127].
+// ---------------------------------------------------------------------------------------
+constexpr float kRht32Scale = 0.17677669529663688f;   // RN(1/sqrt(32)) = 0x3E3504F3
+
+__device__ __forceinline__ void fwht32(float (&v)[32]) {
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if ((i & h) == 0) {
+                const float a = v[i], b = v[i + h];
+                v[i] = __fadd_rn(a, b);
+                v[i + h] = __fsub_rn(a, b);
+            }
+        }
+    }
+}
+
+// forward: signs, butterflies, scale
+__device__ __forceinline__ void rht32_forward(float (&v)[32], uint32_t signs) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(__float_as_uint(v[i]) ^ (((signs >> i) & 1u) << 31));
+    fwht32(v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], kRht32Scale);
+}
+
+// inverse: butterflies, scale, signs
+__device__ __forceinline__ void rht32_inverse(float (&v)[32], uint32_t signs) {
+    fwht32(v);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        v[i] = __uint_as_float(__float_as_uint(__fmul_rn(v[i], kRht32Scale)) ^ (((signs >> i) & 1u) << 31));
+}
+
+// S2F6 block exponent (ceiling rule with the format's maximum 127/64 = 1.111111b):
+// amax = m 2^E, m in [1, 2): e = E + (m > 127/64); subnormal amax: -127 up to 127 * 2^-133.
+__device__ __forceinline__ int s2f6_exponent(float amax) {
+    const uint32_t u = __float_as_uint(amax) & 0x7FFFFFFFu;
+    if (u < 0x00800000u) return u <= 0x007F0000u ? -127 : -126;
+    const int e = (int)(u >> 23) - 127 + ((u & 0x7FFFFFu) > 0x7E0000u ? 1 : 0);
+    return e > 127 ? 127 : e;
+}
+
+// 32 rotated values -> 32 S2F6 bytes (out, 8 words) and the E8M0 byte.
+__device__ __forceinline__ uint32_t s2f6_encode32(const float (&y)[32], uint32_t (&out)[8]) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(y[i]));
+    const int e = s2f6_exponent(amax);
+    const float inv = exp2i(-e);        // y 2^-e, then x 64: both exact (a value that is
+                                        // subnormal after the first step is < 2^-120 and rounds to 0)
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        int q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int t = __float2int_rn(__fmul_rn(__fmul_rn(y[4 * w + j], inv), 64.0f));
+            q[j] = min(max(t, -128), 127);
+        }
+        out[w] = __byte_perm(__byte_perm((uint32_t)q[0], (uint32_t)q[1], 0x0040u),
+                             __byte_perm((uint32_t)q[2], (uint32_t)q[3], 0x0040u), 0x5410u);
+    }
+    return (uint32_t)(e + 127);
+}
+
+// one S2F6 word (4 codes) with E8M0 byte sc -> 4 exact fp32 values
+__device__ __forceinline__ void s2f6_decode4(uint32_t word, uint32_t sc, float* out) {
+    const float step = exp2i_wide((int)sc - 127 - 6);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) out[j] = __fmul_rn((float)(int8_t)(word >> (8 * j)), step);
+}
+
 }  // namespace fp4q

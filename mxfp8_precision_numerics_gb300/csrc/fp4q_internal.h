@@ -36,6 +36,10 @@ struct RequantArgs {
     uint8_t* out_e8m0;
 };
 cudaError_t launch_requant(const RequantArgs& a, cudaStream_t st);
+cudaError_t launch_combine_encode(const void* in, int in_bf16, int64_t rows, int64_t cols, uint32_t signs,
+                                  uint8_t* codes, uint8_t* e8m0, cudaStream_t st);
+cudaError_t launch_combine_decode(const uint8_t* codes, const uint8_t* e8m0, int64_t tokens, int64_t k,
+                                  int64_t cols, uint32_t signs, void* out, int out_bf16, cudaStream_t st);
 cudaError_t launch_rht16(const void* in, int in_is_bf16, float* out, int64_t rows, int64_t cols,
                          uint32_t signs, cudaStream_t st);
 
@@ -53,12 +57,14 @@ struct GemmArgs {
     int64_t M, N, K;
     int groups;
     const int64_t* group_offsets;   // host, groups + 1 (NULL when groups == 1)
-    // epilogue (bf16 output only): 0 plain; 1 GELU: d = h, d2 = GELU(h), amax_out = max|d2|;
-    // 2 GELU backward: d = bf16(d_bf16 * GELU'(aux)), aux = the layer's pre-activation h
+    // epilogue: 0 plain; 1 GELU (bf16): d = h, d2 = GELU(h), amax_out = max|d2|;
+    // 2 GELU backward (bf16): d = bf16(d_bf16 * GELU'(aux)), aux = the layer's pre-activation h;
+    // 3 combine encode (d_bf16 = 0): RHT32 + S2F6 of each row's groups of 32
     int epi = 0;
     void* d2 = nullptr;
     const uint16_t* aux = nullptr;
     float* amax_out = nullptr;   // epi 1; may be NULL
+    uint32_t rht32_signs = 0;    // epi 3: combine encode (d = S2F6 bytes, d2 = E8M0 per 32), fp32 path
     int a_sdec_rows = 0;         // NVFP4: A carries one outer scale per row
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st);

@@ -92,7 +92,9 @@ struct Params {
     int groups;
     int64_t goff[65];
     int gtile[65];
-    int epi;                   // 0 plain, 1 GELU (d = h, d2 = GELU(h), amax), 2 GELU backward
+    int epi;                   // 0 plain, 1 GELU (d = h, d2 = GELU(h), amax), 2 GELU backward,
+                               // 3 combine encode (d = S2F6 bytes, d2 = E8M0 per 32)
+    uint32_t rht32_signs;      // epi 3
     void* d2;
     const uint16_t* aux;
     float* amax_out;
@@ -358,6 +360,23 @@ __device__ __forceinline__ void epi_flush_amax(const Params& p, uint32_t amax_bi
     if (lane == 0 && amax_bits) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), amax_bits << 16);
 }
 
+// Combine-encode epilogue (epi 3): one row's 32 accumulator columns x alpha, rotated (RHT32)
+// and quantized to S2F6 with their E8M0 scale (4bit.vizuara.ai §11: done at the very end of
+// the GEMM so the output never sits in memory in a 16-bit form). N % 32 == 0.
+__device__ __forceinline__ void combine_chunk(const Params& p, const uint32_t (&r)[32], int64_t row, int64_t col,
+                                              float alpha) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(r[i]), alpha);
+    rht32_forward(v, p.rht32_signs);
+    uint32_t q[8];
+    const uint32_t sc = s2f6_encode32(v, q);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.d) + row * p.N + col);
+    dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    static_cast<uint8_t*>(p.d2)[row * (p.N >> 5) + (col >> 5)] = (uint8_t)sc;
+}
+
 // Epilogue of one 128 x 256 accumulator: warp w (TMEM lane quarter w) loads rows
 // m0 + 32w + lane, 32 columns at a time, scales by alpha and stores fp32 or bf16.
 __device__ __forceinline__ void store_tile(const Params& p, uint32_t tacc, int warp, int lane, int64_t m0,
@@ -378,6 +397,10 @@ __device__ __forceinline__ void store_tile(const Params& p, uint32_t tacc, int w
             continue;
         }
         if (!row_ok || col >= p.N) continue;
+        if (p.epi == 3) {
+            combine_chunk(p, r, row, col, alpha);
+            continue;
+        }
         const bool full32 = col + 32 <= p.N;
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.N + col);
 #pragma unroll
@@ -839,6 +862,10 @@ __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32
 __device__ __forceinline__ void store_chunk(const Params& p, const uint32_t (&r)[32], int64_t row, bool row_ok,
                                             int64_t col, float alpha) {
     if (!row_ok || col >= p.N) return;
+    if (p.epi == 3) {
+        combine_chunk(p, r, row, col, alpha);
+        return;
+    }
     const bool full32 = col + 32 <= p.N;
     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.d) + row * p.N + col);
 #pragma unroll
@@ -852,7 +879,10 @@ __device__ __forceinline__ void store_chunk(const Params& p, const uint32_t (&r)
 }
 
 // Output tile `tile` of the pair -> this CTA's first row and the tile's first column.
-__device__ __forceinline__ void pair_tile(const Params& p, int tile, uint32_t rank, int64_t& m0, int64_t& n0) {
+// Grouped GEMMs: the 256-row tiles of group g are gtile[g] .. gtile[g+1]-1, starting at row
+// goff[g]; the rows of a group's last tile past goff[g+1] belong to the next group (or lie past
+// M) and are computed but not stored. Returns the group.
+__device__ __forceinline__ int pair_tile(const Params& p, int tile, uint32_t rank, int64_t& m0, int64_t& n0) {
     int mt, nt;
     if (p.m_fastest) {
         nt = tile / p.m_tiles;
@@ -861,8 +891,11 @@ __device__ __forceinline__ void pair_tile(const Params& p, int tile, uint32_t ra
         mt = tile / p.n_tiles;
         nt = tile - mt * p.n_tiles;
     }
-    m0 = (int64_t)mt * 256 + 128 * (int64_t)rank;
+    int g = 0;
+    while (g + 1 < p.groups && p.gtile[g + 1] <= mt) ++g;
+    m0 = p.goff[g] + (int64_t)(mt - p.gtile[g]) * 256 + 128 * (int64_t)rank;
     n0 = (int64_t)nt * kBN;
+    return g;
 }
 
 // Persistent CTA-pair GEMM: cluster c computes tiles c, c + C, c + 2C, ... (C clusters).
@@ -941,9 +974,9 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         const int total_units = my_tiles * units_per_tile;
         // The scale stream runs ahead of the A/B stream; both track their tile incrementally
         // (a runtime division per K-block on this lane would hold back the TMA issue).
-        int sf_u = 0, sf_uk = 0, sf_ti = 0;
+        int sf_u = 0, sf_uk = 0, sf_ti = 0, sf_g = 0;
         int64_t sf_m0 = 0, sf_n0 = 0;
-        if (total_units > 0) pair_tile(p, cid, rank, sf_m0, sf_n0);
+        if (total_units > 0) sf_g = pair_tile(p, cid, rank, sf_m0, sf_n0);
         // next scale unit into staging slot sf_u % R, once the writers have read that slot's
         // previous unit
         auto load_next_sf = [&]() -> bool {
@@ -953,21 +986,25 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
                 uint8_t* dst = sf_stage + r * kSfUnit;
                 mbar_arrive_expect_tx(&sf_full[r], kSfUnitA + (p.b_sc_2d ? 16u : (uint32_t)kBN) * kW);
                 tma_load_2d(&p.tma_sfa, &sf_full[r], dst, sf_uk * (int)kW, (int32_t)sf_m0);
+                const int64_t brow = (int64_t)sf_g * p.N + sf_n0;   // the group's B rows
                 tma_load_2d(&p.tma_sfb, &sf_full[r], dst + kSfUnitA, sf_uk * (int)kW,
-                            (int32_t)(p.b_sc_2d ? (sf_n0 >> 4) : sf_n0));
+                            (int32_t)(p.b_sc_2d ? (brow >> 4) : brow));
             }
             ++sf_u;
             if (++sf_uk == units_per_tile) {
                 sf_uk = 0;
-                if (++sf_ti < my_tiles) pair_tile(p, cid + sf_ti * ncl, rank, sf_m0, sf_n0);
+                if (++sf_ti < my_tiles) sf_g = pair_tile(p, cid + sf_ti * ncl, rank, sf_m0, sf_n0);
             }
             return true;
         };
         bool ok = true;
         int issued = 0;
-        int64_t m0 = 0, n0 = 0;
+        int64_t m0 = 0, n0 = 0, brow = 0;
         for (int gk = 0, kb = 0, ti = 0; gk < total_kb && ok; ++gk) {
-            if (kb == 0) pair_tile(p, cid + ti * ncl, rank, m0, n0);
+            if (kb == 0) {
+                const int g = pair_tile(p, cid + ti * ncl, rank, m0, n0);
+                brow = (int64_t)g * p.N + n0 + 128 * rank;
+            }
             while (ok && sf_u < total_units && sf_u <= gk / G + DU) ok = load_next_sf();
             if (!ok) break;
             const int s = gk % S;
@@ -977,7 +1014,7 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
                 if (leader) mbar_arrive_expect_tx(&full[s], 2 * kPairStage);
                 const uint32_t bar = leader_addr(&full[s]);
                 tma_load_2d_pair_hint(&p.tma_a, bar, st, kb * kBKBytes, (int32_t)m0, pol_a);
-                tma_load_2d_pair_hint(&p.tma_b, bar, st + kABytes, kb * kBKBytes, (int32_t)(n0 + 128 * rank), pol_b);
+                tma_load_2d_pair_hint(&p.tma_b, bar, st + kABytes, kb * kBKBytes, (int32_t)brow, pol_b);
             }
             issued = gk + 1;
             if (++kb == p.num_kb) {
@@ -1066,14 +1103,14 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         const uint32_t tacc = tmem + kAccCol + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
         const uint32_t empty_leader = leader_addr(tmem_empty);
         const bool rows_sd = kKind == 0 && p.a_sdec_rows;
-        const float b_sd = kKind == 0 ? p.b_s_dec[0] : 1.0f;
-        const float alpha_t = kKind == 0 && !rows_sd ? __fmul_rn(p.a_s_dec[0], b_sd) : 1.0f;
         uint32_t amax_bits = 0;
         for (int ti = 0; ti < my_tiles; ++ti) {
             int64_t m0, n0;
-            pair_tile(p, cid + ti * ncl, rank, m0, n0);
+            const int g = pair_tile(p, cid + ti * ncl, rank, m0, n0);
             const int64_t row = m0 + 32 * q + lane;
-            const bool row_ok = row < p.M;
+            const bool row_ok = row < p.goff[g + 1];
+            const float b_sd = kKind == 0 ? p.b_s_dec[g] : 1.0f;
+            const float alpha_t = kKind == 0 && !rows_sd ? __fmul_rn(p.a_s_dec[0], b_sd) : 1.0f;
             // per-row outer scale of A: loaded before the wait for the accumulator
             const float alpha = rows_sd ? (row_ok ? __fmul_rn(p.a_s_dec[row], b_sd) : 0.0f) : alpha_t;
             if (!mbar_wait_idle(accum_full, (uint32_t)ti & 1u)) break;
@@ -1205,6 +1242,7 @@ cudaError_t launch_kind(const GemmArgs& a, cudaStream_t st) {
     p.d = a.d;
     p.d_bf16 = a.d_bf16;
     p.epi = a.epi;
+    p.rht32_signs = a.rht32_signs;
     p.d2 = a.d2;
     p.aux = a.aux;
     p.amax_out = a.amax_out;
@@ -1234,7 +1272,7 @@ cudaError_t launch_kind(const GemmArgs& a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-// The CTA-pair kernel for one group and M > 128: clusters of 2 CTAs over 256-row blocks.
+// The CTA-pair kernel: clusters of 2 CTAs over 256-row blocks (of each group).
 template <int kKind>
 cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
     static int configured_device = -1;
@@ -1250,14 +1288,15 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
     memset(&p, 0, sizeof(p));
     const uint64_t kbytes = kKind == 0 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
     if (!make_map(&p.tma_a, a.a, kbytes, (uint64_t)a.M, kBM)) return cudaErrorInvalidValue;
-    if (!make_map(&p.tma_b, a.b, kbytes, (uint64_t)a.N, 128)) return cudaErrorInvalidValue;
+    if (!make_map(&p.tma_b, a.b, kbytes, (uint64_t)a.N * (uint64_t)a.groups, 128)) return cudaErrorInvalidValue;
     const uint64_t sc_ld = kKind == 0 ? (uint64_t)a.K / 16 : (uint64_t)a.K / 32;
     const bool b2d = kKind == 0 && a.b_scale_kind == 2;
+    const uint64_t b_rows = (uint64_t)a.N * (uint64_t)a.groups;
     // NVFP4 scale rows (64 bytes) land with the 64-byte swizzle the writers read them through
     const CUtensorMapSwizzle sf_swz = kKind == 0 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE;
     if (!make_map_sf(&p.tma_sfa, a.a_scales, sc_ld, (uint64_t)a.M, sf_unit_w<kKind>(), kBM, sf_swz))
         return cudaErrorInvalidValue;
-    if (!make_map_sf(&p.tma_sfb, a.b_scales, sc_ld, b2d ? (uint64_t)a.N / 16 : (uint64_t)a.N, sf_unit_w<kKind>(),
+    if (!make_map_sf(&p.tma_sfb, a.b_scales, sc_ld, b2d ? b_rows / 16 : b_rows, sf_unit_w<kKind>(),
                      b2d ? 16 : kBN, sf_swz))
         return cudaErrorInvalidValue;
     p.a_sc = a.a_scales;
@@ -1270,6 +1309,7 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
     p.d = a.d;
     p.d_bf16 = a.d_bf16;
     p.epi = a.epi;
+    p.rht32_signs = a.rht32_signs;
     p.d2 = a.d2;
     p.aux = a.aux;
     p.amax_out = a.amax_out;
@@ -1278,9 +1318,19 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
     p.K = a.K;
     p.num_kb = (int)(a.K / Cfg<kKind>::kValuesPerStage);
     p.n_tiles = (int)((a.N + kBN - 1) / kBN);
-    p.m_tiles = (int)((a.M + 255) / 256);
-    p.groups = 1;
-    const double a_bytes = (double)a.M * (double)kbytes, b_bytes = (double)a.N * (double)kbytes;
+    p.groups = a.groups;
+    int64_t tiles_m = 0;
+    for (int gi = 0; gi < a.groups; ++gi) {
+        const int64_t lo = a.groups == 1 ? 0 : a.group_offsets[gi];
+        const int64_t hi = a.groups == 1 ? a.M : a.group_offsets[gi + 1];
+        p.goff[gi] = lo;
+        p.gtile[gi] = (int)tiles_m;
+        tiles_m += (hi - lo + 255) / 256;
+    }
+    p.goff[a.groups] = a.M;
+    p.gtile[a.groups] = (int)tiles_m;
+    p.m_tiles = (int)tiles_m;
+    const double a_bytes = (double)a.M * (double)kbytes, b_bytes = (double)b_rows * (double)kbytes;
     p.m_fastest = a_bytes < b_bytes ? 1 : 0;
     const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
     static int max_clusters[2] = {0, 0};
@@ -1304,9 +1354,9 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-// Kernel choice: the CTA pair for single-group GEMMs with more than one 128-row tile and a main
-// loop of at least 32 stages (it halves each SM's B stream but has a longer per-tile prologue
-// and epilogue); the single-CTA kernel for grouped GEMMs, short K and M <= 128.
+// Kernel choice: the persistent CTA pair (grouped or not) whenever the scale TMA applies (scale
+// rows of a multiple of 16 bytes, whole scale units per tile, 16-byte aligned scale pointers)
+// and the GEMM is grouped or has more than one 128-row tile; the single-CTA kernel otherwise.
 #ifndef FP4Q_GEMM_PAIR
 #define FP4Q_GEMM_PAIR 1
 #endif
@@ -1325,7 +1375,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     const int64_t g_units = a.kind == 0 ? Pair<0>::G : Pair<1>::G;
     const bool sf_tma = sc_ld % 16 == 0 && stages % g_units == 0 &&
                         ((reinterpret_cast<uintptr_t>(a.a_scales) | reinterpret_cast<uintptr_t>(a.b_scales)) & 15u) == 0;
-    if (FP4Q_GEMM_PAIR && a.groups == 1 && a.M > 128 && stages >= FP4Q_PAIR_MIN_STAGES && sf_tma)
+    if (FP4Q_GEMM_PAIR && (a.groups > 1 || a.M > 128) && stages >= FP4Q_PAIR_MIN_STAGES && sf_tma)
         return a.kind == 0 ? launch_pair<0>(a, st) : launch_pair<1>(a, st);
     return a.kind == 0 ? launch_kind<0>(a, st) : launch_kind<1>(a, st);
 }

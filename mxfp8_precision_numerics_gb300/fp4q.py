@@ -60,6 +60,10 @@ _SIGS = {
     "fp4q_gemm_nvfp4_gelu_rows": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
                                          _vp]),
     "fp4q_gemm_mxfp8_dgelu": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "fp4q_combine_encode": (_int, [_vp, _int, _i64, _i64, _u32, _vp, _vp, _vp]),
+    "fp4q_combine_decode": (_int, [_vp, _vp, _i64, _i64, _i64, _u32, _vp, _int, _vp]),
+    "fp4q_gemm_nvfp4_combine": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _u32, _vp, _vp, _i64, _i64, _i64,
+                                       _int, _vp, _vp]),
     "fp4q_device_status": (_int, [_vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -186,6 +190,26 @@ def fp4q_gemm_mxfp8_dgelu(a, a_scales, b, b_scales, h, dh_out, M, N, K, stream=N
                                       M, N, K, _stream(stream)), "fp4q_gemm_mxfp8_dgelu")
 
 
+def fp4q_combine_encode(x, x_dtype, rows, cols, rht_signs, codes, e8m0, stream=None):
+    _check(_lib.fp4q_combine_encode(_ptr(x), x_dtype, rows, cols, int(rht_signs), _ptr(codes), _ptr(e8m0),
+                                    _stream(stream)), "fp4q_combine_encode")
+
+
+def fp4q_combine_decode(codes, e8m0, tokens, k, cols, rht_signs, out, out_dtype, stream=None):
+    _check(_lib.fp4q_combine_decode(_ptr(codes), _ptr(e8m0), tokens, k, cols, int(rht_signs), _ptr(out),
+                                    out_dtype, _stream(stream)), "fp4q_combine_decode")
+
+
+def fp4q_gemm_nvfp4_combine(a, a_scales, a_s_dec, b, b_scales, b_scale_kind, b_s_dec, rht_signs, codes_out,
+                            e8m0_out, M, N, K, groups=1, group_row_offsets=None, stream=None):
+    keep, offs = _offsets(group_row_offsets)
+    _check(_lib.fp4q_gemm_nvfp4_combine(_ptr(a), _ptr(a_scales), _ptr(a_s_dec), _ptr(b), _ptr(b_scales),
+                                        b_scale_kind, _ptr(b_s_dec), int(rht_signs), _ptr(codes_out),
+                                        _ptr(e8m0_out), M, N, K, groups, offs, _stream(stream)),
+           "fp4q_gemm_nvfp4_combine")
+    del keep
+
+
 def fp4q_device_status(stream=None):
     return _lib.fp4q_device_status(_stream(stream))
 
@@ -308,6 +332,36 @@ def gemm_mxfp8_dgelu(a, a_scales, b, b_scales, h, stream=None):
     dh = _empty((M, N), torch.bfloat16, a.device)
     fp4q_gemm_mxfp8_dgelu(a, a_scales, b, b_scales, h, dh, M, N, K, stream)
     return dh
+
+
+def combine_encode(x, rht_signs, stream=None):
+    """fp32 or bf16 [rows, cols] -> (S2F6 codes u8 [rows, cols], e8m0 u8 [rows, cols/32])."""
+    rows, cols = x.shape
+    codes = _empty((rows, cols), torch.uint8, x.device)
+    e8 = _empty((rows, cols // 32), torch.uint8, x.device)
+    fp4q_combine_encode(x, BF16 if x.dtype == torch.bfloat16 else F32, rows, cols, rht_signs, codes, e8, stream)
+    return codes, e8
+
+
+def combine_decode(codes, e8m0, k, rht_signs, out_dtype=torch.float32, stream=None):
+    """[tokens*k, cols] arrivals -> [tokens, cols]: each token's k arrivals summed, rotated back."""
+    rows, cols = codes.shape
+    out = _empty((rows // k, cols), out_dtype, codes.device)
+    fp4q_combine_decode(codes, e8m0, rows // k, k, cols, rht_signs, out,
+                        BF16 if out_dtype == torch.bfloat16 else F32, stream)
+    return out
+
+
+def gemm_nvfp4_combine(a, a_scales, a_s_dec, b, b_scales, b_scale_kind, b_s_dec, rht_signs, groups=1,
+                       group_row_offsets=None, stream=None):
+    """gemm_nvfp4 whose output leaves in the combine wire format -> (codes [M, N], e8m0 [M, N/32])."""
+    M, K = a.shape[0], a.shape[1] * 2
+    N = b.shape[-2]
+    codes = _empty((M, N), torch.uint8, a.device)
+    e8 = _empty((M, N // 32), torch.uint8, a.device)
+    fp4q_gemm_nvfp4_combine(a, a_scales, a_s_dec, b, b_scales, b_scale_kind, b_s_dec, rht_signs, codes, e8,
+                            M, N, K, groups, group_row_offsets, stream)
+    return codes, e8
 
 
 def gemm_mxfp8(a, a_scales, b, b_scales, out_dtype=torch.float32, stream=None):

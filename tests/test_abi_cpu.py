@@ -123,6 +123,24 @@ def test_validation_rejects_bad_arguments_without_touching_cuda(F):
     assert qr(q, 16, 32, 32, 1, p, p, p, n) == F.ERR_ALIGN
     assert qr(p, 16, 32, 36, 1, p, p, p, n) == F.ERR_ALIGN                             # ld % 8
     assert qr(p, 16, 32, 32, 1, p, p, p, n) in (F.ERR_CUDA, F.ERR_UNSUPPORTED)        # valid, no GPU
+    # combine codec
+    ce = L.fp4q_combine_encode
+    assert ce(p, 2, 4, 64, 0, p, p, n) == F.ERR_ARG                                    # dtype
+    assert ce(p, 0, 4, 48, 0, p, p, n) == F.ERR_SHAPE                                  # cols % 32
+    assert ce(p, 0, 0, 64, 0, p, p, n) == F.ERR_SHAPE
+    assert ce(p, 0, 4, 64, 0, n, p, n) == F.ERR_NULL
+    assert ce(q, 0, 4, 64, 0, p, p, n) == F.ERR_ALIGN
+    cd = L.fp4q_combine_decode
+    assert cd(p, p, 4, 0, 64, 0, p, 0, n) == F.ERR_SHAPE                               # k
+    assert cd(p, p, 4, 2, 40, 0, p, 0, n) == F.ERR_SHAPE
+    assert cd(p, p, 4, 2, 64, 0, p, 3, n) == F.ERR_ARG
+    assert cd(p, n, 4, 2, 64, 0, p, 0, n) == F.ERR_NULL
+    assert cd(p, p, 4, 2, 64, 0, q, 0, n) == F.ERR_ALIGN
+    gc = L.fp4q_gemm_nvfp4_combine
+    assert gc(p, p, p, p, p, 2, p, 0, p, p, 128, 48, 256, 1, None, n) == F.ERR_SHAPE  # N % 32
+    assert gc(p, p, p, p, p, 2, p, 0, p, n, 128, 64, 256, 1, None, n) == F.ERR_NULL
+    assert gc(p, p, p, p, p, 3, p, 0, p, p, 128, 64, 256, 1, None, n) == F.ERR_ARG
+    assert gc(p, p, p, p, p, 2, p, 0, q, p, 128, 64, 256, 1, None, n) == F.ERR_ALIGN
     dg = L.fp4q_gemm_mxfp8_dgelu
     assert dg(p, p, p, p, n, p, 128, 256, 128, n) == F.ERR_NULL                        # no h
     assert dg(p, p, p, p, p, p, 128, 250, 128, n) == F.ERR_SHAPE                       # N % 16

@@ -164,6 +164,33 @@ def test_nvfp4_grouped_equals_per_group(F, orc):
         assert_gemm_close(d[lo:hi], ref, f"group {g}")
 
 
+@pytest.mark.parametrize("two_d,out_dtype", [(True, torch.float32), (False, torch.float32), (True, torch.bfloat16)])
+def test_nvfp4_grouped_pair_kernel(F, orc, two_d, out_dtype):
+    """Grouped GEMMs on the persistent CTA-pair kernel (K a multiple of 1024): ragged groups, an
+    empty group, groups smaller than a 128-row half tile, a ragged N."""
+    rng = np.random.default_rng(17 + two_d)
+    G, N, K = 5, 272, 1024
+    rows = [300, 0, 37, 500, 256]
+    offs = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    M = int(offs[-1])
+    a, asc = rand_nvfp4(rng, M, K)
+    bs = [rand_nvfp4(rng, N, K, two_d) for _ in range(G)]
+    b = np.stack([x[0] for x in bs])
+    bsc = np.stack([x[1] for x in bs])
+    bsd = np.array([0.5, 0.25, 2.0, 1.0, 0.125], np.float32)
+    d = run_nvfp4(F, a, asc, 0.75, b, bsc, 2 if two_d else 1, bsd, out_dtype, groups=G, offs=list(offs))
+    got = d.float().cpu().numpy()
+    for g in range(G):
+        lo, hi = offs[g], offs[g + 1]
+        if hi == lo:
+            continue
+        ref = orc.gemm_nvfp4(a[lo:hi], asc[lo:hi], 1, 0.75, b[g], bsc[g], 2 if two_d else 1, float(bsd[g]))
+        if out_dtype == torch.float32:
+            assert_gemm_close(got[lo:hi], ref, f"pair group {g}")
+        else:
+            assert_bf16_rounding_of(d[lo:hi].cpu().view(torch.int16).numpy().view(np.uint16), ref, f"pair group {g}")
+
+
 def test_nvfp4_single_linear_config(F, orc):
     """Config: X 256x512 (+outliers), W 256x512, Y = X W^T 256x256 fp32, seed 0."""
     x = I.normal_with_outliers(256, 512, seed=0)

@@ -128,9 +128,11 @@ def test_gemm_nvfp4_rows(F, orc, M, N, K, two_d):
                       f"NVFP4 rows {M}x{N}x{K}")
 
 
-def test_gemm_nvfp4_rows_grouped(F, orc):
-    rng = np.random.default_rng(9)
-    G, N, K = 3, 64, 512
+@pytest.mark.parametrize("K", [512, 1024])
+def test_gemm_nvfp4_rows_grouped(F, orc, K):
+    """K = 512: the single-CTA kernel; K = 1024: the grouped CTA-pair kernel."""
+    rng = np.random.default_rng(9 + K)
+    G, N = 3, 64
     offs = [0, 100, 100, 260]
     M = offs[-1]
     a, asc = rand_nvfp4(rng, M, K)
