@@ -690,3 +690,46 @@ EXPORT void orc_combine_decode(const uint8_t* codes, const uint8_t* e8m0, int64_
             for (int i = 0; i < 32; ++i) out[t * cols + g * 32 + i] = acc[i];
         }
 }
+
+/* ------------------------------------------------------------------------- */
+/* MXFP4 (the Open Compute microscaling format the pages compare NVFP4 with): */
+/* E2M1 codes, one E8M0 power-of-two scale per 32 consecutive values of a row. */
+/* [AC] "The scaling math, worked": scale = 2^ceil(log2(amax / 6)), q =       */
+/* round_to_E2M1(x / scale) (amax 22 -> scale 4, 22 -> 5.5 -> 6 -> 24);       */
+/* [NV] "NVFP4 Format and Quantization Procedure" / App. B.4 on MXFP4 (a block */
+/* with amax 3 + delta keeps 3 as its largest code); [NV] Section 5: MXFP4    */
+/* pairs with 32-point Hadamard transforms.                                  */
+/* Readings: the ceiling exponent is orc_pow2_ceil_exponent(amax, 6) (the     */
+/* MXFP8 rule with the E2M1 maximum), clamped to [-127, 127]; codes are RNE   */
+/* ties to even (as NVFP4); with rht the row's groups of 32 are rotated by    */
+/* orc_rht32_group first (in fp32) and the rotated values are quantized.     */
+/* codes [rows][cols/2] (element 2j low nibble), e8m0 [rows][cols/32].        */
+/* ------------------------------------------------------------------------- */
+EXPORT void orc_quantize_mxfp4(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int rht,
+                               uint32_t signs, uint8_t* codes, uint8_t* e8m0)
+{
+    float v[32];
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t g = 0; g < cols / 32; ++g) {
+            for (int i = 0; i < 32; ++i) v[i] = bf16_value(x[r * ld + g * 32 + i]);
+            if (rht) orc_rht32_group(v, signs);
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) if (fabs((double)v[i]) > amax) amax = fabs((double)v[i]);
+            int e = orc_pow2_ceil_exponent(amax, 6.0);
+            e8m0[r * (cols / 32) + g] = (uint8_t)(e + 127);
+            for (int i = 0; i < 32; ++i) {
+                float t = (float)ldexp((double)v[i], -e);      /* exact power-of-two scaling */
+                put_code(codes, cols / 2, r, g * 32 + i, orc_e2m1_encode_rne(t));
+            }
+        }
+}
+
+/* MXFP4 dequantize: code x 2^(e8m0 - 127), exact in double. */
+EXPORT void orc_dequant_mxfp4(const uint8_t* codes, const uint8_t* e8m0, int64_t rows, int64_t cols,
+                              double* out)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c)
+            out[r * cols + c] = orc_e2m1_decode(get_code(codes, cols / 2, r, c))
+                                * ldexp(1.0, (int)e8m0[r * (cols / 32) + c / 32] - 127);
+}

@@ -106,6 +106,10 @@ def lib():
         L.orc_combine_encode.argtypes = [ctypes.c_void_p, ctypes.c_int, _i64, _i64, ctypes.c_uint32, _u8p, _u8p]
         L.orc_combine_decode.restype = None
         L.orc_combine_decode.argtypes = [_u8p, _u8p, _i64, _i64, _i64, ctypes.c_uint32, _f32p]
+        L.orc_quantize_mxfp4.restype = None
+        L.orc_quantize_mxfp4.argtypes = [_u16p, _i64, _i64, _i64, ctypes.c_int, ctypes.c_uint32, _u8p, _u8p]
+        L.orc_dequant_mxfp4.restype = None
+        L.orc_dequant_mxfp4.argtypes = [_u8p, _u8p, _i64, _i64, _f64p]
         _LIB = L
     return _LIB
 
@@ -367,6 +371,33 @@ def combine_decode(codes, e8m0, k, signs):
     out = np.zeros((rows // k, cols), np.float32)
     lib().orc_combine_decode(_p(codes, _u8p), _p(e8m0, _u8p), rows // k, k, cols, int(signs), _p(out, _f32p))
     return out
+
+
+# ---------------------------------------------------------------- MXFP4
+def quantize_mxfp4(x, rht=False, signs=0):
+    """bf16 bits [rows, cols] -> (codes [rows, cols/2], e8m0 [rows, cols/32]); rht rotates each
+    group of 32 first."""
+    x = _c(x, np.uint16)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    e8 = np.zeros((rows, cols // 32), np.uint8)
+    lib().orc_quantize_mxfp4(_p(x, _u16p), rows, cols, cols, int(bool(rht)), int(signs), _p(codes, _u8p),
+                             _p(e8, _u8p))
+    return codes, e8
+
+
+def dequant_mxfp4(codes, e8m0):
+    codes = _c(codes, np.uint8)
+    e8m0 = _c(e8m0, np.uint8)
+    rows, cols = codes.shape[0], codes.shape[1] * 2
+    out = np.zeros((rows, cols), np.float64)
+    lib().orc_dequant_mxfp4(_p(codes, _u8p), _p(e8m0, _u8p), rows, cols, _p(out, _f64p))
+    return out
+
+
+def gemm_mxfp4(a_codes, a_e8m0, b_codes, b_e8m0):
+    """D = A . B^T on exactly dequantized MXFP4 operands, float64."""
+    return dequant_mxfp4(a_codes, a_e8m0) @ dequant_mxfp4(b_codes, b_e8m0).T
 
 
 # ---------------------------------------------------------------- GEMMs

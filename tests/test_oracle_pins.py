@@ -836,3 +836,74 @@ def test_wire_format_errors_order_like_page(orc, worked):
     spike = lambda b: float(np.max(np.abs(b)) / np.sqrt(np.mean(b ** 2)))
     worst = int(np.argmax([spike(b) for b in blocks]))
     assert spike(rot[worst]) < spike(blocks[worst]) / 2
+
+
+# ------------------------------------------------------------------ MXFP4 (the format comparison)
+def test_mxfp4_worked_examples(orc, worked):
+    """[AC] "The scaling math, worked": amax 22 -> scale 2^ceil(log2(22/6)) = 4, 22 -> 5.5 -> 6 -> 24.
+    [NV] App. B.4: a block with amax 3 + delta keeps 3 as its largest code (power-of-two scale 1),
+    while amax exactly 3 gets scale 1/2 and reaches 6."""
+    ex = worked["pow2_22"]
+    row = [ex["x"]] + [0.0] * 31
+    codes, e8 = orc.quantize_mxfp4(bf16([row]))
+    assert 2.0 ** (int(e8[0, 0]) - 127) == ex["scale"]
+    assert orc.dequant_mxfp4(codes, e8)[0, 0] == ex["deq"]
+    codes, e8 = orc.quantize_mxfp4(bf16([[3.015625] + [0.0] * 31]))
+    assert e8[0, 0] == 127 and orc.dequant_mxfp4(codes, e8)[0, 0] == 3.0
+    codes, e8 = orc.quantize_mxfp4(bf16([[3.0] + [0.0] * 31]))
+    assert e8[0, 0] == 126 and (codes[0, 0] & 0x7) == 0x7
+    # a block max of exactly 6 * 2^k keeps scale 2^k and the top code
+    for k in (-20, 0, 9):
+        codes, e8 = orc.quantize_mxfp4(bf16([[6.0 * 2.0 ** k] + [0.0] * 31]))
+        assert e8[0, 0] == 127 + k and (codes[0, 0] & 0x7) == 0x7
+
+
+def test_mxfp4_gemm_brute_force(orc):
+    rng = np.random.default_rng(11)
+    M, N, K = 5, 7, 64
+    ac = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    bc = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    ae = rng.integers(118, 136, (M, K // 32), dtype=np.uint8)
+    be = rng.integers(118, 136, (N, K // 32), dtype=np.uint8)
+    D = orc.gemm_mxfp4(ac, ae, bc, be)
+
+    def code(c, r, k):
+        byte = int(c[r, k // 2])
+        return (byte >> 4) if k % 2 else (byte & 15)
+    for m in range(M):
+        for n in range(N):
+            acc = sum(orc.e2m1_decode(code(ac, m, k)) * 2.0 ** (int(ae[m, k // 32]) - 127)
+                      * orc.e2m1_decode(code(bc, n, k)) * 2.0 ** (int(be[n, k // 32]) - 127) for k in range(K))
+            assert abs(D[m, n] - acc) <= 1e-12 * max(1.0, abs(acc))
+
+
+def test_mxfp4_error_above_nvfp4_and_rht_on_heavy_tails(orc):
+    """The pages' format comparison: power-of-two scales per 32 lose accuracy against E4M3
+    scales per 16 ([NV] "NVFP4 vs. MXFP4"; [AC] micro-scaling). With a 32-point rotation first,
+    MXFP4's error on heavy-tailed data drops ([NV] Section 5 pairs MXFP4 with d = 32)."""
+    x = inputs.normal(64, 1024, seed=41)
+    xb = inputs.bf16_bits(x)
+    xf = x.float().numpy().astype(np.float64)
+    n = np.linalg.norm(xf)
+    c, e = orc.quantize_mxfp4(xb)
+    e_mx = np.linalg.norm(orc.dequant_mxfp4(c, e) - xf) / n
+    c1, s1, _, sd = orc.quantize_1d(xb)
+    e_nv = np.linalg.norm(orc.dequant_nvfp4(c1, s1, 1, sd) - xf) / n
+    assert 0.08 < e_nv < e_mx < 0.14, (e_nv, e_mx)
+    t = inputs.student_t(32, 1024, seed=42, df=3, scale=1.0)
+    tb = inputs.bf16_bits(t)
+    tf = t.float().numpy().astype(np.float32)
+    signs = 0x5EED_1234
+    c, e = orc.quantize_mxfp4(tb)
+    e_plain = np.linalg.norm(orc.dequant_mxfp4(c, e) - tf) / np.linalg.norm(tf)
+    c, e = orc.quantize_mxfp4(tb, rht=True, signs=signs)
+    rot = np.array([orc.rht32_group(b, signs) for b in tf.reshape(-1, 32)]).reshape(tf.shape)
+    e_rht = np.linalg.norm(orc.dequant_mxfp4(c, e) - rot) / np.linalg.norm(rot)
+    assert e_rht < e_plain, (e_rht, e_plain)
+    # with the rotation, a block is the plain MXFP4 rule applied to the rotated values
+    codes, e8 = orc.quantize_mxfp4(tb[:1], rht=True, signs=signs)
+    v = orc.rht32_group(tf[0, :32], signs)
+    sc = 2.0 ** (int(e8[0, 0]) - 127)
+    assert sc == 2.0 ** orc.pow2_ceil_exponent(float(np.abs(v).max()), 6.0)
+    want = [orc.e2m1_encode_rne(np.float32(vi / sc)) for vi in v]
+    assert [int(c) for c in unpack_codes(codes)[0, :32]] == want
