@@ -300,6 +300,32 @@ FP4Q_API int fp4q_gemm_mxfp8_dgelu(const uint8_t* a, const uint8_t* a_scales,
                     int64_t M, int64_t N, int64_t K, fp4q_stream_t stream);
 
 /*
+ * fp4q_quantize_mxfp4 — MXFP4, the Open Compute microscaling format the NVFP4 paper compares
+ * against: E2M1 codes with one E8M0 scale per 32 values of a row. [AC] "The scaling math,
+ * worked" (scale = 2^ceil(log2(amax / 6))); [NV] Section 5 and App. B.4.
+ *   per group of 32 (optionally rotated first: rht = 1 applies the RHT32 of the combine format
+ *   below, the 32-point transform the paper pairs with MXFP4): e = the smallest integer with
+ *   amax <= 6 * 2^e, clamped to [-127, 127]; e8m0 = e + 127; code_i = E2M1_RNE(x_i * 2^-e)
+ *   x_bf16    [rows][ld] bf16, 16-byte aligned, ld % 8 == 0
+ *   codes     [rows][cols/2] (element 2j low nibble), 16-byte aligned; e8m0 [rows][cols/32]
+ *   rows >= 1, cols % 32 == 0.
+ */
+FP4Q_API int fp4q_quantize_mxfp4(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld, int rht,
+                    uint32_t rht_signs, uint8_t* codes, uint8_t* e8m0, fp4q_stream_t stream);
+
+/*
+ * fp4q_gemm_mxfp4 — block-scaled MXFP4 x MXFP4 GEMM, D = A . B^T, FP32 accumulation on the
+ * tcgen05 tensor cores (block-scaled E2M1 MMA with UE8M0 scales, two per row and MMA):
+ *   D[m,n] = sum_blk 2^(ea[m,blk]-127) * 2^(eb[n,blk]-127) * sum_{k in blk} a_k b_k
+ *   a, a_e8m0   codes [M][K/2], E8M0 [M][K/32];  b, b_e8m0  codes [N][K/2], E8M0 [N][K/32]
+ *   d, d_dtype  [M][N] FP4Q_F32 or FP4Q_BF16
+ *   M >= 1, N % 16 == 0, K % 2048 == 0 (the kernel stages the scales of 2048 values of K at a
+ *   time); all pointers 16-byte aligned.
+ */
+FP4Q_API int fp4q_gemm_mxfp4(const uint8_t* a, const uint8_t* a_e8m0, const uint8_t* b, const uint8_t* b_e8m0,
+                    void* d, int d_dtype, int64_t M, int64_t N, int64_t K, fp4q_stream_t stream);
+
+/*
  * The MoE combine wire format: RHT32 + block-scaled S2F6 ([VZ] §11, "Combine is harder";
  * [TML] 合并阶段). A layer output is rotated in groups of 32 consecutive values of a row and
  * sent as S2F6 (8.25 bits per value); the receiver sums the dequantized arrivals of a token

@@ -264,6 +264,44 @@ int fp4q_gemm_nvfp4_combine(const uint8_t* a, const uint8_t* a_scales, const flo
     return cuda_status(fp4q::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int fp4q_quantize_mxfp4(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld, int rht, uint32_t rht_signs,
+                        uint8_t* codes, uint8_t* e8m0, fp4q_stream_t stream) {
+    if (rht != 0 && rht != 1) return FP4Q_ERR_ARG;
+    if (!x_bf16 || !codes || !e8m0) return FP4Q_ERR_NULL;
+    if (rows < 1 || cols < 32 || cols % 32 != 0 || ld < cols) return FP4Q_ERR_SHAPE;
+    if (!al16(x_bf16) || ld % 8 != 0 || !al16(codes)) return FP4Q_ERR_ALIGN;
+    if (int d = check_device()) return d;
+    return cuda_status(fp4q::launch_quantize_mxfp4(static_cast<const uint16_t*>(x_bf16), rows, cols, ld, rht,
+                                                   rht_signs, codes, e8m0, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp4q_gemm_mxfp4(const uint8_t* a, const uint8_t* a_e8m0, const uint8_t* b, const uint8_t* b_e8m0,
+                    void* d, int d_dtype, int64_t M, int64_t N, int64_t K, fp4q_stream_t stream) {
+    if (d_dtype != FP4Q_F32 && d_dtype != FP4Q_BF16) return FP4Q_ERR_ARG;
+    if (!a || !a_e8m0 || !b || !b_e8m0 || !d) return FP4Q_ERR_NULL;
+    if (M < 1 || N < 16 || N % 16 != 0 || K < 2048 || K % 2048 != 0) return FP4Q_ERR_SHAPE;
+    if (M > 2147483647 || N > 2147483647) return FP4Q_ERR_SHAPE;
+    if (!al16(a) || !al16(b) || !al16(a_e8m0) || !al16(b_e8m0) || !al16(d)) return FP4Q_ERR_ALIGN;
+    if (int dv = check_device()) return dv;
+    fp4q::GemmArgs g;
+    g.kind = 2;
+    g.a = a;
+    g.a_scales = a_e8m0;
+    g.a_s_dec = nullptr;
+    g.b = b;
+    g.b_scales = b_e8m0;
+    g.b_scale_kind = 1;
+    g.b_s_dec = nullptr;
+    g.d = d;
+    g.d_bf16 = d_dtype == FP4Q_BF16;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.groups = 1;
+    g.group_offsets = nullptr;
+    return cuda_status(fp4q::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fp4q_combine_encode(const void* x, int x_dtype, int64_t rows, int64_t cols, uint32_t rht_signs,
                         uint8_t* codes, uint8_t* e8m0, fp4q_stream_t stream) {
     if (x_dtype != FP4Q_F32 && x_dtype != FP4Q_BF16) return FP4Q_ERR_ARG;

@@ -84,6 +84,7 @@ __device__ __forceinline__ uint32_t e2m1x2_cvt_rn(float lo, float hi) {
 __device__ __forceinline__ int mx_exponent(float amax) {
     uint32_t u = __float_as_uint(amax) & 0x7FFFFFFFu;
     if (u < 0x00800000u) return -127;             // zero or subnormal: far below 448*2^-127
+    if (u >= 0x7F800000u) return 127;             // infinite: no e fits, the clamp
     int E = (int)(u >> 23) - 127;
     int e = E - 8 + ((u & 0x7FFFFFu) > 0x600000u ? 1 : 0);
     return e < -127 ? -127 : (e > 127 ? 127 : e);

@@ -16,6 +16,8 @@ cudaError_t launch_quantize_1d(const uint16_t* x, int64_t rows, int64_t cols, in
 cudaError_t launch_quantize_1d_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int four_six,
                                     uint8_t* codes, uint8_t* scales, float* s_dec_rows, cudaStream_t st);
 void rows_shape(int64_t cols, int& W, int& hold);   // warps per row, blocks per thread
+cudaError_t launch_quantize_mxfp4(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int rht, uint32_t signs,
+                                  uint8_t* codes, uint8_t* e8m0, cudaStream_t st);
 cudaError_t launch_quantize_2d(const uint16_t* w, int64_t rows, int64_t cols, int64_t ld,
                                int64_t batch, int64_t batch_stride, const float* amax,
                                uint8_t* codes, uint8_t* tile_scales, float* s_dec,
@@ -44,7 +46,7 @@ cudaError_t launch_rht16(const void* in, int in_is_bf16, float* out, int64_t row
                          uint32_t signs, cudaStream_t st);
 
 struct GemmArgs {
-    int kind;                    // 0 NVFP4, 1 MXFP8
+    int kind;                    // 0 NVFP4, 1 MXFP8, 2 MXFP4 (E8M0 scales per 32; K % 2048 == 0)
     const uint8_t* a;
     const uint8_t* a_scales;
     const float* a_s_dec;        // NVFP4 only: one float, or [M] when a_sdec_rows

@@ -58,6 +58,11 @@ template <> struct Cfg<1> {   // MXFP8: K = 128 values per stage, 4 MMAs of K = 
     static constexpr uint32_t kSfRowBytes = 4;        // 4 scales per row and stage
     static constexpr int kValuesPerStage = 128;
 };
+template <> struct Cfg<2> {   // MXFP4 (CTA-pair kernel only): K = 256 values per stage, 4 MMAs of K = 64
+    static constexpr uint32_t kSfColsPerStage = 24;   // SFA 2 x 4 cols + SFB 2 x 8 cols (2 bytes per MMA)
+    static constexpr uint32_t kSfRowBytes = 8;        // 8 E8M0 scales per row and stage
+    static constexpr int kValuesPerStage = 256;
+};
 
 constexpr uint32_t kABytes = kBM * kBKBytes;      // 16 KB
 constexpr uint32_t kBBytes = kBN * kBKBytes;      // 32 KB
@@ -561,6 +566,13 @@ __device__ __forceinline__ void mma2_nvfp4(uint32_t d, uint64_t a, uint64_t b, u
                  " [%0], %1, %2, %3, [%5], [%6], p;}"
                  ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb) : "memory");
 }
+__device__ __forceinline__ void mma2_mxfp4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t sfa, uint32_t sfb, uint32_t acc) {
+    asm volatile("{.reg .pred p; setp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X"
+                 " [%0], %1, %2, %3, [%5], [%6], p;}"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb) : "memory");
+}
 __device__ __forceinline__ void mma2_mxfp8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                            uint32_t sfa, uint32_t sfb, uint32_t acc) {
     asm volatile("{.reg .pred p; setp.ne.b32 p, %4, 0;\n"
@@ -760,6 +772,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 template <int kKind> struct Pair;
 template <> struct Pair<0> { static constexpr int S = 5, G = 4, R = 2, DU = 1, T = 5; };
 template <> struct Pair<1> { static constexpr int S = 6, G = 4, R = 3, DU = 2, T = 16; };
+// MXFP4: units of 8 K-blocks, so that a unit's scale rows are 64 bytes like NVFP4's (same swizzle)
+template <> struct Pair<2> { static constexpr int S = 5, G = 8, R = 2, DU = 1, T = 10; };
+static_assert(256 + Pair<2>::T * Cfg<2>::kSfColsPerStage <= kTmemCols, "MXFP4 scale slots");
 static_assert(256 + Pair<0>::T * Cfg<0>::kSfColsPerStage <= kTmemCols, "NVFP4 scale slots");
 static_assert(256 + Pair<1>::T * Cfg<1>::kSfColsPerStage <= kTmemCols, "MXFP8 scale slots");
 static_assert(Pair<0>::R >= Pair<0>::DU + 1 && Pair<1>::R >= Pair<1>::DU + 1, "scale ring depth");
@@ -781,9 +796,14 @@ __host__ __device__ constexpr uint32_t pair_smem_bytes() {
 }
 static_assert(pair_smem_bytes<0>() <= 227 * 1024, "NVFP4 pair shared memory");
 static_assert(pair_smem_bytes<1>() <= 227 * 1024, "MXFP8 pair shared memory");
+static_assert(pair_smem_bytes<2>() <= 227 * 1024, "MXFP4 pair shared memory");
 constexpr uint32_t kIdesc2Nvfp4 = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                                   (0u << 23) | ((uint32_t)(256 >> 4) << 24);
 constexpr uint32_t kIdesc2Mxfp8 = (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                                  (1u << 23) | ((uint32_t)(256 >> 4) << 24);
+// MXFP4: E2M1 operands, UE8M0 scales, scale_vec::2X (two scale bytes per row and MMA, the
+// pair selected by the scale-factor id 0 or 2)
+constexpr uint32_t kIdesc2Mxfp4 = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                                   (1u << 23) | ((uint32_t)(256 >> 4) << 24);
 
 // Scale writer step of the pair kernel: K-block `sub` of a staged unit (rows W bytes apart)
@@ -798,9 +818,28 @@ __device__ __forceinline__ void write_unit_scales(const uint8_t* unit, int sub, 
     constexpr uint32_t W = sf_unit_w<kKind>();
     const uint8_t* a0 = unit;
     const uint8_t* b0 = unit + sf_unit_a<kKind>();
-    static_assert(kKind != 0 || W == 64, "the NVFP4 swizzle below assumes 64-byte scale rows");
+    static_assert(kKind == 1 || W == 64, "the FP4 swizzle below assumes 64-byte scale rows");
     const int ra = lane + 32 * quarter;
-    if (kKind == 0) {
+    if (kKind == 2) {
+        // MXFP4 units (64-byte rows, same swizzle): K-block `sub` is the 8-byte half sub & 1 of
+        // chunk sub >> 1. Word 0 (scales 0-3) serves MMAs 0 and 1, word 1 (scales 4-7) MMAs 2 and 3
+        // (scale-factor ids 0 and 2 pick the byte pair). SFA: columns sf + quarter, sf + 4 +
+        // quarter; SFB: columns sf + 8 + c and sf + 16 + c (c = row / 32).
+        const int ch = sub >> 1;
+        const uint4 a = *reinterpret_cast<const uint4*>(a0 + ra * W + 16 * (ch ^ ((ra >> 1) & 3)));
+        uint32_t b0w[8], b1w[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int r = lane + 32 * c;
+            const uint4 v = *reinterpret_cast<const uint4*>(b0 + r * W + 16 * (ch ^ ((r >> 1) & 3)));
+            b0w[c] = (sub & 1) ? v.z : v.x;
+            b1w[c] = (sub & 1) ? v.w : v.y;
+        }
+        tmem_st1(sf + 0 + quarter, (sub & 1) ? a.z : a.x);
+        tmem_st1(sf + 4 + quarter, (sub & 1) ? a.w : a.y);
+        tmem_st8(sf + 8, b0w);
+        tmem_st8(sf + 16, b1w);
+    } else if (kKind == 0) {
         // NVFP4 units arrive with the TMA's 64-byte swizzle: the 16-byte chunk `sub` of row r
         // sits at chunk sub ^ ((r >> 1) & 3), so the 8 lanes of a quarter-warp read 8 distinct
         // bank groups
@@ -1054,6 +1093,14 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
                         for (int j = 0; j < 4; ++j)
                             mma2_nvfp4(tmem + kAccCol, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
                                        kIdesc2Nvfp4, sf_col + 4 * j, sf_col + 16 + 8 * j, (kb | j) ? 1u : 0u);
+                    } else if (kKind == 2) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t id = 2u * (uint32_t)(j & 1);
+                            mma2_mxfp4(tmem + kAccCol, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
+                                       kIdesc2Mxfp4 | (id << 29) | (id << 4), sf_col + 4 * (j >> 1),
+                                       sf_col + 8 + 8 * (j >> 1), (kb | j) ? 1u : 0u);
+                        }
                     } else {
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
@@ -1286,14 +1333,14 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
     }
     Params p;
     memset(&p, 0, sizeof(p));
-    const uint64_t kbytes = kKind == 0 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
+    const uint64_t kbytes = kKind != 1 ? (uint64_t)a.K / 2 : (uint64_t)a.K;      // FP4: two codes per byte
     if (!make_map(&p.tma_a, a.a, kbytes, (uint64_t)a.M, kBM)) return cudaErrorInvalidValue;
     if (!make_map(&p.tma_b, a.b, kbytes, (uint64_t)a.N * (uint64_t)a.groups, 128)) return cudaErrorInvalidValue;
     const uint64_t sc_ld = kKind == 0 ? (uint64_t)a.K / 16 : (uint64_t)a.K / 32;
     const bool b2d = kKind == 0 && a.b_scale_kind == 2;
     const uint64_t b_rows = (uint64_t)a.N * (uint64_t)a.groups;
     // NVFP4 scale rows (64 bytes) land with the 64-byte swizzle the writers read them through
-    const CUtensorMapSwizzle sf_swz = kKind == 0 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const CUtensorMapSwizzle sf_swz = kKind != 1 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE;
     if (!make_map_sf(&p.tma_sfa, a.a_scales, sc_ld, (uint64_t)a.M, sf_unit_w<kKind>(), kBM, sf_swz))
         return cudaErrorInvalidValue;
     if (!make_map_sf(&p.tma_sfb, a.b_scales, sc_ld, b2d ? b_rows / 16 : b_rows, sf_unit_w<kKind>(),
@@ -1333,7 +1380,7 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
     const double a_bytes = (double)a.M * (double)kbytes, b_bytes = (double)b_rows * (double)kbytes;
     p.m_fastest = a_bytes < b_bytes ? 1 : 0;
     const int64_t tiles = (int64_t)p.m_tiles * p.n_tiles;
-    static int max_clusters[2] = {0, 0};
+    static int max_clusters[3] = {0, 0, 0};
     if (max_clusters[kKind] <= 0) {
         cudaLaunchConfig_t cfg;
         memset(&cfg, 0, sizeof(cfg));
@@ -1368,6 +1415,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
         const cudaError_t e = cudaMemsetAsync(a.amax_out, 0, sizeof(float), st);
         if (e != cudaSuccess) return e;
     }
+    if (a.kind == 2) return launch_pair<2>(a, st);   // MXFP4: K % 2048 == 0 (checked by the caller)
     const int64_t stages = a.K / (a.kind == 0 ? Cfg<0>::kValuesPerStage : Cfg<1>::kValuesPerStage);
     // the pair kernel's scale TMA wants 16-byte aligned scale rows
     const int64_t sc_ld = a.kind == 0 ? a.K / 16 : a.K / 32;

@@ -481,4 +481,74 @@ cudaError_t launch_quantize_1d_rows(const uint16_t* x, int64_t rows, int64_t col
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------------------
+// MXFP4 quantize ("FP4 Training on Blackwell", "The scaling math, worked"; the format the
+// NVFP4 paper compares against): E2M1 codes with one E8M0 scale per 32 values of a row,
+// scale 2^e with e the smallest integer such that amax <= 6 * 2^e (clamped to [-127, 127]).
+// One thread per group of 32 (four 16-byte loads), optionally rotated by RHT32 first (the
+// 32-point transform the paper pairs with MXFP4); codes by the hardware E2M1 conversion of the
+// exactly scaled values; 16 code bytes and one scale byte per thread.
+// ---------------------------------------------------------------------------------------
+// 6 = 1.5 * 2^2: amax = m 2^E (m in [1, 2)) -> e = E - 2 + (m > 1.5); subnormal amax -> -127;
+// an infinite amax satisfies no e and takes the clamp, 127.
+__device__ __forceinline__ int mxfp4_exponent(float amax) {
+    const uint32_t u = __float_as_uint(amax) & 0x7FFFFFFFu;
+    if (u < 0x00800000u) return -127;
+    if (u >= 0x7F800000u) return 127;
+    const int e = (int)(u >> 23) - 127 - 2 + ((u & 0x7FFFFFu) > 0x400000u ? 1 : 0);
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+template <bool kRht>
+__global__ void __launch_bounds__(256) quantize_mxfp4_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                             int64_t cols, int64_t ld, uint32_t signs,
+                                                             uint8_t* __restrict__ codes,
+                                                             uint8_t* __restrict__ e8m0) {
+    const int64_t gpr = cols >> 5;
+    const int64_t groups = rows * gpr;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += stride) {
+        const int64_t r = g / gpr, c = g - r * gpr;
+        const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + c * 32);
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 p = __ldcs(src + q);
+            const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                v[8 * q + 2 * k] = __uint_as_float(w[k] << 16);
+                v[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+            }
+        }
+        if (kRht) rht32_forward(v, signs);
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const int e = mxfp4_exponent(amax);
+        const float inv = exp2i(-e);          // v * 2^-e is exact (|result| <= 6)
+        uint32_t out[4];
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+            uint32_t b[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                b[j] = e2m1x2_cvt_rn(__fmul_rn(v[8 * wd + 2 * j], inv), __fmul_rn(v[8 * wd + 2 * j + 1], inv));
+            out[wd] = pack_bytes4(b[0], b[1], b[2], b[3]);
+        }
+        __stcs(reinterpret_cast<uint4*>(codes + r * (cols >> 1) + c * 16), make_uint4(out[0], out[1], out[2], out[3]));
+        e8m0[g] = (uint8_t)(e + 127);
+    }
+}
+
+cudaError_t launch_quantize_mxfp4(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int rht, uint32_t signs,
+                                  uint8_t* codes, uint8_t* e8m0, cudaStream_t st) {
+    const int g = grid_for(rows * (cols / 32), 256);
+    if (rht)
+        quantize_mxfp4_kernel<true><<<g, 256, 0, st>>>(x, rows, cols, ld, signs, codes, e8m0);
+    else
+        quantize_mxfp4_kernel<false><<<g, 256, 0, st>>>(x, rows, cols, ld, signs, codes, e8m0);
+    return cudaGetLastError();
+}
+
 }  // namespace fp4q

@@ -60,6 +60,8 @@ _SIGS = {
     "fp4q_gemm_nvfp4_gelu_rows": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
                                          _vp]),
     "fp4q_gemm_mxfp8_dgelu": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "fp4q_quantize_mxfp4": (_int, [_vp, _i64, _i64, _i64, _int, _u32, _vp, _vp, _vp]),
+    "fp4q_gemm_mxfp4": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp]),
     "fp4q_combine_encode": (_int, [_vp, _int, _i64, _i64, _u32, _vp, _vp, _vp]),
     "fp4q_combine_decode": (_int, [_vp, _vp, _i64, _i64, _i64, _u32, _vp, _int, _vp]),
     "fp4q_gemm_nvfp4_combine": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _u32, _vp, _vp, _i64, _i64, _i64,
@@ -188,6 +190,16 @@ def fp4q_gemm_nvfp4_gelu_rows(a, a_scales, a_s_dec_rows, b, b_scales, b_scale_ki
 def fp4q_gemm_mxfp8_dgelu(a, a_scales, b, b_scales, h, dh_out, M, N, K, stream=None):
     _check(_lib.fp4q_gemm_mxfp8_dgelu(_ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), _ptr(h), _ptr(dh_out),
                                       M, N, K, _stream(stream)), "fp4q_gemm_mxfp8_dgelu")
+
+
+def fp4q_quantize_mxfp4(x, rows, cols, ld, rht, rht_signs, codes, e8m0, stream=None):
+    _check(_lib.fp4q_quantize_mxfp4(_ptr(x), rows, cols, ld, int(rht), int(rht_signs), _ptr(codes), _ptr(e8m0),
+                                    _stream(stream)), "fp4q_quantize_mxfp4")
+
+
+def fp4q_gemm_mxfp4(a, a_e8m0, b, b_e8m0, d, d_dtype, M, N, K, stream=None):
+    _check(_lib.fp4q_gemm_mxfp4(_ptr(a), _ptr(a_e8m0), _ptr(b), _ptr(b_e8m0), _ptr(d), d_dtype, M, N, K,
+                                _stream(stream)), "fp4q_gemm_mxfp4")
 
 
 def fp4q_combine_encode(x, x_dtype, rows, cols, rht_signs, codes, e8m0, stream=None):
@@ -332,6 +344,23 @@ def gemm_mxfp8_dgelu(a, a_scales, b, b_scales, h, stream=None):
     dh = _empty((M, N), torch.bfloat16, a.device)
     fp4q_gemm_mxfp8_dgelu(a, a_scales, b, b_scales, h, dh, M, N, K, stream)
     return dh
+
+
+def quantize_mxfp4(x, rht=False, rht_signs=0, stream=None):
+    """bf16 [rows, cols] -> (codes u8 [rows, cols/2], e8m0 u8 [rows, cols/32])."""
+    rows, cols = x.shape
+    codes = _empty((rows, cols // 2), torch.uint8, x.device)
+    e8 = _empty((rows, cols // 32), torch.uint8, x.device)
+    fp4q_quantize_mxfp4(x, rows, cols, x.stride(0), rht, rht_signs, codes, e8, stream)
+    return codes, e8
+
+
+def gemm_mxfp4(a, a_e8m0, b, b_e8m0, out_dtype=torch.float32, stream=None):
+    M, K = a.shape[0], a.shape[1] * 2
+    N = b.shape[0]
+    d = _empty((M, N), out_dtype, a.device)
+    fp4q_gemm_mxfp4(a, a_e8m0, b, b_e8m0, d, BF16 if out_dtype == torch.bfloat16 else F32, M, N, K, stream)
+    return d
 
 
 def combine_encode(x, rht_signs, stream=None):

@@ -123,6 +123,18 @@ def test_validation_rejects_bad_arguments_without_touching_cuda(F):
     assert qr(q, 16, 32, 32, 1, p, p, p, n) == F.ERR_ALIGN
     assert qr(p, 16, 32, 36, 1, p, p, p, n) == F.ERR_ALIGN                             # ld % 8
     assert qr(p, 16, 32, 32, 1, p, p, p, n) in (F.ERR_CUDA, F.ERR_UNSUPPORTED)        # valid, no GPU
+    # MXFP4
+    qm = L.fp4q_quantize_mxfp4
+    assert qm(p, 4, 64, 64, 2, 0, p, p, n) == F.ERR_ARG
+    assert qm(p, 4, 48, 48, 0, 0, p, p, n) == F.ERR_SHAPE
+    assert qm(p, 4, 64, 64, 0, 0, p, n, n) == F.ERR_NULL
+    assert qm(p, 4, 64, 68, 0, 0, p, p, n) == F.ERR_ALIGN
+    gm = L.fp4q_gemm_mxfp4
+    assert gm(p, p, p, p, p, 0, 128, 256, 1024, n) == F.ERR_SHAPE                    # K % 2048
+    assert gm(p, p, p, p, p, 0, 128, 24, 2048, n) == F.ERR_SHAPE
+    assert gm(p, p, p, p, p, 2, 128, 256, 2048, n) == F.ERR_ARG
+    assert gm(p, n, p, p, p, 0, 128, 256, 2048, n) == F.ERR_NULL
+    assert gm(p, ctypes.c_void_p(20), p, p, p, 0, 128, 256, 2048, n) == F.ERR_ALIGN
     # combine codec
     ce = L.fp4q_combine_encode
     assert ce(p, 2, 4, 64, 0, p, p, n) == F.ERR_ARG                                    # dtype
