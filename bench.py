@@ -8,8 +8,9 @@ first one's epilogue); four MXFP8 requants with stochastic rounding (two with th
 RHT) and two MXFP8 GEMMs per layer backward (GELU' in the second layer's dgrad epilogue).
 The metric is the step's dense GEMM throughput (6 x 2 M D F FLOPs per step) in TFLOP/s.
 The line also reports the same step with the activations quantized per token row with
-Four Over Six block scales ("per_token_4over6"), timed separately, and the MoE combine wire
-format (RHT32 + S2F6) at the MoE layer's size ("combine_codec").
+Four Over Six block scales ("per_token_4over6"), timed separately, the MoE combine wire
+format (RHT32 + S2F6) at the MoE layer's size ("combine_codec"), and MXFP4 beside NVFP4 on the
+weight sweep's largest shape ("mxfp4_vs_nvfp4").
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -57,6 +58,9 @@ BYTES_PER_ELEM = {
     "combine_encode_bf16": 2.0 + 1 + 1 / 32,
     "combine_decode_k1_f32": 1 + 1 / 32 + 4.0,
     "combine_decode_k2_bf16": 2 * (1 + 1 / 32) + 2.0,
+    # MXFP4 (one pass: E8M0 per 32 needs no tensor amax)
+    "quantize_mxfp4": 2.0 + 0.5 + 1 / 32,
+    "quantize_mxfp4_rht32": 2.0 + 0.5 + 1 / 32,
 }
 
 
@@ -248,7 +252,8 @@ def summarize_kernels(kinds, peaks):
         avg = tot_ms / n
         if kind.startswith("gemm"):
             tf = units / (tot_ms * 1e-3) / 1e12
-            peak = peaks["bf16_tflops_sustained"] * (RATIO_FP4 if kind.startswith("gemm_nvfp4") else RATIO_FP8)
+            fp4 = kind.startswith(("gemm_nvfp4", "gemm_mxfp4"))
+            peak = peaks["bf16_tflops_sustained"] * (RATIO_FP4 if fp4 else RATIO_FP8)
             kernels[kind] = {"launches": n, "avg_ms": round(avg, 4), "achieved": round(tf, 1),
                              "unit": "TFLOP/s", "peak": round(peak, 1), "frac": round(tf / peak, 4)}
         else:
@@ -303,6 +308,44 @@ def combine_section(F, torch, dev, peaks, iters=10):
         raise RuntimeError("device status after the combine section: " + F.status_str(st))
     return {"workload": f"MoE combine: {T} tokens x d_model {D}, {E} experts x {T // E} tokens (top-1), "
                         f"expert ffn {FE}; decode k=2 on {2 * T} arrivals; inputs N(0,1) / Student-t(3)",
+            "iterations": iters, "kernels": summarize_kernels(log.totals(), peaks)}
+
+
+def format_section(F, torch, dev, peaks, iters=10):
+    """MXFP4 beside NVFP4 on the weight sweep's largest shape (X 16384 x 4096, W 14336 x 4096):
+    the activation quantizers and the bf16-output GEMMs."""
+    from mxfp8_precision_numerics_gb300 import inputs as I
+    M, N, K = 16384, 14336, 4096
+    signs = 0x5EED1234
+    x = I.normal_with_outliers(M, K, seed=3).to(dev)
+    w = I.normal(N, K, seed=30, std=0.02).to(dev)
+    xc, xs, xsd, _ = F.quantize_1d(x)
+    wc, ws, wsd, _ = F.quantize_2d(w)
+    mxc, mxe = F.quantize_mxfp4(x)
+    mwc, mwe = F.quantize_mxfp4(w)
+    log = EventLog(torch)
+    L = log.wrap
+    flops = 2.0 * M * N * K
+
+    def once():
+        L("quantize_1d", M * K, F.quantize_1d, x)
+        L("quantize_mxfp4", M * K, F.quantize_mxfp4, x)
+        L("quantize_mxfp4_rht32", M * K, F.quantize_mxfp4, x, True, signs)
+        L("gemm_nvfp4_w2d", flops, F.gemm_nvfp4, xc, xs, xsd, wc, ws, F.SCALE_2D, wsd, torch.bfloat16)
+        L("gemm_mxfp4", flops, F.gemm_mxfp4, mxc, mxe, mwc, mwe, torch.bfloat16)
+
+    for _ in range(3):
+        once()
+    torch.cuda.synchronize()
+    log.on = True
+    for _ in range(iters):
+        once()
+    torch.cuda.synchronize()
+    log.on = False
+    st = F.fp4q_device_status()
+    if st != F.OK:
+        raise RuntimeError("device status after the format section: " + F.status_str(st))
+    return {"workload": f"X {M}x{K} N(0,1)+0.1% x50, W {N}x{K} N(0,0.02); bf16 GEMM outputs",
             "iterations": iters, "kernels": summarize_kernels(log.totals(), peaks)}
 
 
@@ -500,6 +543,7 @@ def run_ours(args, rank, world, local_rank):
         },
     }
     res["combine_codec"] = combine_section(F, torch, dev, peaks)
+    res["mxfp4_vs_nvfp4"] = format_section(F, torch, dev, peaks)
     if world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.cpu_sample)
     if dist is not None:

@@ -20,8 +20,9 @@ def _e4m3(shape, g):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--call", required=True,
-                    choices=["gemm_mxfp8", "gemm_nvfp4", "quantize_1d", "quantize_2d", "requant_bf16_t_rht",
-                             "requant_bf16_rows", "requant_nvfp4_t_rht", "requant_nvfp4_2d_t"])
+                    choices=["gemm_mxfp8", "gemm_nvfp4", "gemm_nvfp4_gelu", "gemm_mxfp4", "quantize_1d", "quantize_2d",
+                             "quantize_1d_rows46", "quantize_mxfp4", "requant_bf16_t_rht", "requant_bf16_rows",
+                             "requant_nvfp4_t_rht", "requant_nvfp4_2d_t", "combine_encode", "combine_decode"])
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--N", type=int, default=4096)
     ap.add_argument("--K", type=int, default=16384)
@@ -35,17 +36,37 @@ def main():
         As = torch.randint(120, 134, (M, K // 32), dtype=torch.uint8, device="cuda", generator=g)
         Bs = torch.randint(120, 134, (N, K // 32), dtype=torch.uint8, device="cuda", generator=g)
         fn = lambda: F.gemm_mxfp8(A, As, B, Bs, torch.bfloat16)
-    elif a.call == "gemm_nvfp4":
+    elif a.call in ("gemm_nvfp4", "gemm_nvfp4_gelu"):
         A = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device="cuda", generator=g)
         B = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda", generator=g)
         As = torch.randint(0x18, 0x58, (M, K // 16), dtype=torch.uint8, device="cuda", generator=g)
         Bs = torch.randint(0x18, 0x58, (N // 16, K // 16), dtype=torch.uint8, device="cuda", generator=g)
         one = torch.ones(1, device="cuda")
-        fn = lambda: F.gemm_nvfp4(A, As, one, B, Bs, F.SCALE_2D, one, torch.bfloat16)
+        if a.call == "gemm_nvfp4":
+            fn = lambda: F.gemm_nvfp4(A, As, one, B, Bs, F.SCALE_2D, one, torch.bfloat16)
+        else:
+            fn = lambda: F.gemm_nvfp4_gelu(A, As, one, B, Bs, F.SCALE_2D, one)
+    elif a.call == "gemm_mxfp4":
+        A = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device="cuda", generator=g)
+        B = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda", generator=g)
+        As = torch.randint(118, 136, (M, K // 32), dtype=torch.uint8, device="cuda", generator=g)
+        Bs = torch.randint(118, 136, (N, K // 32), dtype=torch.uint8, device="cuda", generator=g)
+        fn = lambda: F.gemm_mxfp4(A, As, B, Bs, torch.bfloat16)
+    elif a.call in ("combine_encode", "combine_decode"):
+        y = torch.randn(M, K, device="cuda", generator=g)
+        codes, e8 = F.combine_encode(y, 0x9E3779B9)
+        if a.call == "combine_encode":
+            fn = lambda: F.combine_encode(y, 0x9E3779B9)
+        else:
+            fn = lambda: F.combine_decode(codes, e8, 1, 0x9E3779B9, torch.float32)
     else:
         x = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
         if a.call == "quantize_1d":
             fn = lambda: F.quantize_1d(x)
+        elif a.call == "quantize_1d_rows46":
+            fn = lambda: F.quantize_1d_rows(x, True)
+        elif a.call == "quantize_mxfp4":
+            fn = lambda: F.quantize_mxfp4(x)
         elif a.call == "quantize_2d":
             fn = lambda: F.quantize_2d(x)
         elif a.call == "requant_bf16_t_rht":
