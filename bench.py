@@ -409,12 +409,14 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- end to end through the public API with host buffers (pinned)
     # Every step copies its inputs in from pinned host memory and its results (Y, dX, dW1, dW2)
-    # back out, as a training loop feeding the layer from the host would: a copy stream brings
-    # step i+1's inputs in while step i computes and takes step i's results out as they are
-    # done. Device buffers and pinned result buffers are allocated before the timed loop. The
-    # device events and the host wall clock bracket the loop.
+    # back out, as a training loop feeding the layer from the host would: one copy stream brings
+    # step i+1's inputs in while step i computes, another takes step i's results out as they are
+    # done (the two directions use separate copy engines and run at the same time). Device
+    # buffers and pinned result buffers are allocated before the timed loop. The device events
+    # and the host wall clock bracket the loop.
     e2e_steps = max(1, args.steps // 2)
-    copy = torch.cuda.Stream(device=dev)
+    copy = torch.cuda.Stream(device=dev)          # host -> device
+    copy_out = torch.cuda.Stream(device=dev)      # device -> host
     comp = torch.cuda.current_stream(dev)
     dbuf = [[torch.empty_like(t, device=dev) for t in host] for _ in range(2)]
     outs_host = None
@@ -436,22 +438,24 @@ def run_ours(args, rank, world, local_rank):
             outs = mlp_step(F, torch, dbuf[b], log, seed, signs)
             buf_free[b].record(comp)
             out_done.record(comp)
-            with torch.cuda.stream(copy):
-                if i + 1 < nsteps:
+            if i + 1 < nsteps:
+                with torch.cuda.stream(copy):
                     nb = (i + 1) % 2
                     if i >= 1:
                         copy.wait_event(buf_free[nb])
                     for d, hsrc in zip(dbuf[nb], host):
                         d.copy_(hsrc, non_blocking=True)
                     in_ready[nb].record(copy)
-                copy.wait_event(out_done)
+            with torch.cuda.stream(copy_out):
+                copy_out.wait_event(out_done)
                 if outs_host is None:
                     outs_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
                 for oh, o in zip(outs_host, outs):
-                    o.record_stream(copy)
+                    o.record_stream(copy_out)
                     oh.copy_(o, non_blocking=True)
             d2h = sum(o.numel() * o.element_size() for o in outs)
         comp.wait_stream(copy)
+        comp.wait_stream(copy_out)
 
     e2e_loop(2)                      # warm-up: allocations and first-touch outside the timing
     torch.cuda.synchronize()
