@@ -229,3 +229,20 @@ def test_linear_layer_with_per_token_activations(F, orc):
     assert np.linalg.norm(y.cpu().numpy() - ref) / np.linalg.norm(ref) < 0.15
     assert dx.shape == (M, K) and dw.shape == (N, K)
     assert torch.isfinite(dx.float()).all() and torch.isfinite(dw).all()
+
+
+def test_readme_example_runs(F):
+    """The usage example of the repository's front page, as written there."""
+    from mxfp8_precision_numerics_gb300 import layer
+    x = torch.randn(4096, 4096, device="cuda").to(torch.bfloat16)
+    w = (0.02 * torch.randn(4096, 4096, device="cuda")).to(torch.bfloat16)
+    y, saved = layer.linear_forward(x, w, out_dtype=torch.bfloat16, outer="row")
+    dy = torch.randn_like(y)
+    dx, dw = layer.linear_backward(dy, saved, seed=1234, rht_signs=0xA5C3)
+    codes, scales, s_dec, amax = F.quantize_1d(x)
+    wc, wt, ws_dec, _ = F.quantize_2d(w)
+    d = F.gemm_nvfp4(codes, scales, s_dec, wc, wt, F.SCALE_2D, ws_dec, torch.float32)
+    assert F.fp4q_device_status() == F.OK
+    ref = x.float() @ w.float().t()
+    assert float((d - ref).norm() / ref.norm()) < 0.15 and float((y.float() - ref).norm() / ref.norm()) < 0.15
+    assert dx.shape == x.shape and dw.shape == w.shape
