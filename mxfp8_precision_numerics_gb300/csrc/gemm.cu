@@ -1156,6 +1156,16 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
             const bool row_ok = row < p.goff[g + 1];
             const float b_sd = kKind == 0 ? p.b_s_dec[g] : 1.0f;
             const float alpha_t = kKind == 0 && !rows_sd ? __fmul_rn(p.a_s_dec[0], b_sd) : 1.0f;
+            if (p.epi == 2 && row_ok) {
+                // GELU backward reads this thread's 128 columns of h after the accumulator is
+                // out: bring its whole 128-byte lines into L2 now, while the tile's MMAs run
+                const int64_t c0 = n0 + 128 * h;
+                const uint16_t* hp = p.aux + row * p.N + c0;
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    if (c0 + 64 * (k + 1) <= p.N)
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(hp + 64 * k));
+            }
             // per-row outer scale of A: loaded before the wait for the accumulator
             const float alpha = rows_sd ? (row_ok ? __fmul_rn(p.a_s_dec[row], b_sd) : 0.0f) : alpha_t;
             if (!mbar_wait_idle(accum_full, (uint32_t)ti & 1u)) break;
