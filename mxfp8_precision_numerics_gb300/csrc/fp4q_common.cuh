@@ -202,14 +202,32 @@ __device__ __forceinline__ uint32_t bf16_sign_mask2(uint32_t signs, int p) {
 }
 
 // ---------------------------------------------------------------------------------------
+// cp.async (16 bytes, zero-filled when !valid) into shared memory, its commit and wait.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kN>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(kN) : "memory"); }
+
+// ---------------------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
-// SC'11): ten rounds of two 32x32->64 multiplies with the Weyl key schedule.
+// SC'11): ten rounds of two 32x32->64 multiplies with the Weyl key schedule. Each product
+// is one mul.wide.u32 (its low and high words are the round's lo and hi).
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        uint64_t p0, p1;
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c.x), "r"(0xD2511F53u));
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c.z), "r"(0xCD9E8D57u));
+        const uint32_t lo0 = (uint32_t)p0, hi0 = (uint32_t)(p0 >> 32);
+        const uint32_t lo1 = (uint32_t)p1, hi1 = (uint32_t)(p1 >> 32);
         c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
@@ -327,25 +345,33 @@ __device__ __forceinline__ uint32_t s2f6_encode32(const float (&y)[32], uint32_t
     const int e = s2f6_exponent(amax);
     const float inv = exp2i(-e);        // y 2^-e, then x 64: both exact (a value that is
                                         // subnormal after the first step is < 2^-120 and rounds to 0)
+    // Clamp to [-128, 127], then round half to even by adding 1.5 * 2^23: in [2^23, 2^24) the
+    // spacing is 1, so the sum is 1.5 * 2^23 + RNE(t) and its low byte is RNE(t) in two's
+    // complement (clamping first or last gives the same code). No integer conversion is needed.
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-        int q[4];
+        uint32_t b[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int t = __float2int_rn(__fmul_rn(__fmul_rn(y[4 * w + j], inv), 64.0f));
-            q[j] = min(max(t, -128), 127);
+            const float t = __fmul_rn(__fmul_rn(y[4 * w + j], inv), 64.0f);
+            b[j] = __float_as_uint(__fadd_rn(fminf(fmaxf(t, -128.0f), 127.0f), 12582912.0f));
         }
-        out[w] = __byte_perm(__byte_perm((uint32_t)q[0], (uint32_t)q[1], 0x0040u),
-                             __byte_perm((uint32_t)q[2], (uint32_t)q[3], 0x0040u), 0x5410u);
+        out[w] = __byte_perm(__byte_perm(b[0], b[1], 0x0040u), __byte_perm(b[2], b[3], 0x0040u), 0x5410u);
     }
     return (uint32_t)(e + 127);
 }
 
-// one S2F6 word (4 codes) with E8M0 byte sc -> 4 exact fp32 values
+// one S2F6 word (4 codes) with E8M0 byte sc -> 4 exact fp32 values. Code c (int8) is taken
+// as the float 2^23 + (c + 128) (its biased byte under the exponent bits of 2^23), less
+// 2^23 + 128 (exact), times the power-of-two step (exact).
 __device__ __forceinline__ void s2f6_decode4(uint32_t word, uint32_t sc, float* out) {
     const float step = exp2i_wide((int)sc - 127 - 6);
+    const uint32_t biased = word ^ 0x80808080u;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) out[j] = __fmul_rn((float)(int8_t)(word >> (8 * j)), step);
+    for (int j = 0; j < 4; ++j) {
+        const float f = __uint_as_float(__byte_perm(biased, 0x4B000000u, 0x7440u + j));
+        out[j] = __fmul_rn(__fsub_rn(f, 8388736.0f), step);
+    }
 }
 
 }  // namespace fp4q

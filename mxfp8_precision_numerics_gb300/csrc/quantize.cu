@@ -487,7 +487,9 @@ cudaError_t launch_quantize_1d_rows(const uint16_t* x, int64_t rows, int64_t col
 // scale 2^e with e the smallest integer such that amax <= 6 * 2^e (clamped to [-127, 127]).
 // One thread per group of 32 (four 16-byte loads), optionally rotated by RHT32 first (the
 // 32-point transform the paper pairs with MXFP4); codes by the hardware E2M1 conversion of the
-// exactly scaled values; 16 code bytes and one scale byte per thread.
+// exactly scaled values; 16 code bytes and one scale byte per thread. (A variant that staged
+// 32-group chunks per warp through shared memory by cp.async measured 6-8% slower: this
+// kernel's loads already keep HBM busy and its arithmetic, not memory, is the limit with RHT.)
 // ---------------------------------------------------------------------------------------
 // 6 = 1.5 * 2^2: amax = m 2^E (m in [1, 2)) -> e = E - 2 + (m > 1.5); subnormal amax -> -127;
 // an infinite amax satisfies no e and takes the clamp, 127.
@@ -497,6 +499,26 @@ __device__ __forceinline__ int mxfp4_exponent(float amax) {
     if (u >= 0x7F800000u) return 127;
     const int e = (int)(u >> 23) - 127 - 2 + ((u & 0x7FFFFFu) > 0x400000u ? 1 : 0);
     return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// encode one group of 32 (already rotated if kRht): E2M1 codes (4 words) and the E8M0 byte
+template <bool kRht>
+__device__ __forceinline__ uint32_t mxfp4_group(float (&v)[32], uint32_t signs, uint32_t (&out)[4]) {
+    if (kRht) rht32_forward(v, signs);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int e = mxfp4_exponent(amax);
+    const float inv = exp2i(-e);          // v * 2^-e is exact (|result| <= 6)
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+        uint32_t b[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            b[j] = e2m1x2_cvt_rn(__fmul_rn(v[8 * wd + 2 * j], inv), __fmul_rn(v[8 * wd + 2 * j + 1], inv));
+        out[wd] = pack_bytes4(b[0], b[1], b[2], b[3]);
+    }
+    return (uint32_t)(e + 127);
 }
 
 template <bool kRht>
@@ -521,23 +543,10 @@ __global__ void __launch_bounds__(256) quantize_mxfp4_kernel(const uint16_t* __r
                 v[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
             }
         }
-        if (kRht) rht32_forward(v, signs);
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        const int e = mxfp4_exponent(amax);
-        const float inv = exp2i(-e);          // v * 2^-e is exact (|result| <= 6)
         uint32_t out[4];
-#pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {
-            uint32_t b[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                b[j] = e2m1x2_cvt_rn(__fmul_rn(v[8 * wd + 2 * j], inv), __fmul_rn(v[8 * wd + 2 * j + 1], inv));
-            out[wd] = pack_bytes4(b[0], b[1], b[2], b[3]);
-        }
+        const uint32_t sc = mxfp4_group<kRht>(v, signs, out);
         __stcs(reinterpret_cast<uint4*>(codes + r * (cols >> 1) + c * 16), make_uint4(out[0], out[1], out[2], out[3]));
-        e8m0[g] = (uint8_t)(e + 127);
+        e8m0[g] = (uint8_t)sc;
     }
 }
 

@@ -203,14 +203,6 @@ __device__ __forceinline__ void mx_encode_half(float (&v)[16], bool valid, uint6
 // ---------------------------------------------------------------------------------------
 constexpr int kTR = 64, kTC = 128, kTThreads = 256;
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int kN>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(kN) : "memory"); }
-
 template <int kKind>
 struct TStage {
     static constexpr uint32_t kBytes = kKind == 0 ? kTR * kTC * 2 : kTR * kTC / 2;   // 16 KB / 4 KB

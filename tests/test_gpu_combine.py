@@ -61,19 +61,40 @@ def test_encode_degenerate_values(F, orc):
         check_encode(F, orc, x, f"degenerate signs={signs:#x}", signs)
 
 
-@pytest.mark.parametrize("k", [1, 2, 3])
-@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-def test_decode_sums_arrivals(F, orc, k, out_dtype):
-    tokens, cols = 37, 160
-    x = I.student_t(tokens * k, cols, seed=10 + k, df=3, scale=1.0).float()
+def check_decode(F, orc, tokens, k, cols, out_dtype, seed, e8m0_offset=0):
+    x = I.student_t(tokens * k, cols, seed=seed, df=3, scale=1.0).float()
     oc, oe = orc.combine_encode(x.numpy(), SIGNS)
-    out = F.combine_decode(cu(oc), cu(oe), k, SIGNS, out_dtype)
+    e8 = cu(oe)
+    if e8m0_offset:                      # the same scales at an address that is not 4-byte aligned
+        buf = torch.zeros(oe.size + e8m0_offset, dtype=torch.uint8, device="cuda")
+        buf[e8m0_offset:] = e8.flatten()
+        e8 = buf[e8m0_offset:].view(oe.shape)
+        assert e8.data_ptr() % 4 != 0
+    out = F.combine_decode(cu(oc), e8, k, SIGNS, out_dtype)
     torch.cuda.synchronize()
     ref = orc.combine_decode(oc, oe, k, SIGNS)
     if out_dtype == torch.bfloat16:
         ref = orc.round_bf16(ref)
     got = out.float().cpu().numpy()
-    assert np.array_equal(got.view(np.uint32), ref.astype(np.float32).view(np.uint32)), "decode differs"
+    assert np.array_equal(got.view(np.uint32), ref.astype(np.float32).view(np.uint32)), \
+        f"decode differs: tokens {tokens} k {k} cols {cols} {out_dtype}"
+
+
+@pytest.mark.parametrize("k", [1, 2, 3])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("cols", [160, 1024])
+def test_decode_sums_arrivals(F, orc, k, out_dtype, cols):
+    """cols 160: one thread per group; cols 1024: the staged kernel (32-group chunks)."""
+    check_decode(F, orc, 37, k, cols, out_dtype, seed=10 + k)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_decode_many_arrivals_and_unaligned_scales(F, orc, out_dtype):
+    """k = 8 (staged for bf16 output; fp32 output's ring would not fit, so the per-thread
+    kernel), k = 7 (staged for both), and scales at an odd address (per-thread kernel)."""
+    check_decode(F, orc, 9, 8, 2048, out_dtype, seed=31)
+    check_decode(F, orc, 11, 7, 1024, out_dtype, seed=32)
+    check_decode(F, orc, 13, 2, 1024, out_dtype, seed=33, e8m0_offset=1)
 
 
 def test_combine_full_size_sampled(F, orc):

@@ -42,23 +42,28 @@ def check_q(F, orc, x, rht, what, ld_pad=0):
 
 
 @pytest.mark.parametrize("rht", [False, True])
-@pytest.mark.parametrize("rows,cols", [(256, 512), (3, 96), (33, 4096 + 32), (1, 32)])
+@pytest.mark.parametrize("rows,cols", [(256, 512), (3, 96), (33, 4096 + 32), (1, 32), (64, 2048), (5, 1024)])
 def test_quantize_mxfp4_shapes(F, orc, rows, cols, rht):
     check_q(F, orc, I.normal_with_outliers(rows, cols, seed=rows + cols), rht, f"mxfp4 {rows}x{cols} rht={rht}")
 
 
 def test_quantize_mxfp4_padded_and_degenerate(F, orc):
     check_q(F, orc, I.normal(40, 96, seed=3), False, "padded", ld_pad=24)
-    x = torch.zeros(6, 64, dtype=torch.float32)
+    for rht in (False, True):                        # several warps per row, padded rows
+        check_q(F, orc, I.normal_with_outliers(9, 1024, seed=4), rht, f"padded 1024 rht={rht}", ld_pad=40)
+    x = torch.zeros(6, 1024, dtype=torch.float32)
     x[1, 0] = 22.0                                   # the worked example: scale 4, 22 -> 24
     x[2, :32] = 1e-39                                # subnormal block
     x[3, 0] = 3.015625                               # amax 3 + delta keeps 3 as its top code
     x[4, :] = 1.0e37                                 # near the top of the range (its rotation stays finite)
-    x[5, :] = torch.linspace(-6, 6, 64)
-    for rht in (False, True):
-        check_q(F, orc, x.to(torch.bfloat16), rht, f"degenerate rht={rht}")
+    x[5, :] = torch.linspace(-6, 6, 1024)
+    for width in (64, 1024):                         # degenerate rows alone, and among many groups
+        xs = x[:, :width].contiguous()
+        for rht in (False, True):
+            check_q(F, orc, xs.to(torch.bfloat16), rht, f"degenerate {width} rht={rht}")
     x[4, :] = 3.0e38                                 # without the rotation: the largest bf16 values
-    check_q(F, orc, x.to(torch.bfloat16), False, "near-max")
+    for width in (64, 1024):
+        check_q(F, orc, x[:, :width].contiguous().to(torch.bfloat16), False, f"near-max {width}")
 
 
 def rand_mxfp4(rng, rows, k):
