@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(256) combine_decode_kernel(const uint8_t* __re
 // column group c0; its slot holds the k arrivals' 1 KB of codes each (swizzled as 2-piece
 // groups) and then their 32 scale bytes each.
 template <bool kOutBf16, int kStages>
-__global__ void __launch_bounds__(256) combine_decode_staged(const uint8_t* __restrict__ codes,
+__global__ void __launch_bounds__(256, 3) combine_decode_staged(const uint8_t* __restrict__ codes,
                                                              const uint8_t* __restrict__ e8m0,
                                                              int64_t tokens, int k, int64_t gpr,
                                                              uint32_t signs, void* __restrict__ out) {

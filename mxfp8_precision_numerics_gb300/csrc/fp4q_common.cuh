@@ -247,22 +247,60 @@ __device__ __forceinline__ uint32_t slice16(uint4 w, int j) {
 }
 
 // ---------------------------------------------------------------------------------------
+// Packed pairs of fp32 for add/sub/mul/fma.rn.f32x2 (sm_100+): each lane of a packed op
+// rounds exactly like the scalar op; one instruction does two.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t d, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(d));
+}
+
+// ---------------------------------------------------------------------------------------
 // 16-point random Hadamard transform of v[0..15] in place: signs, butterflies at
 // distances 1, 2, 4, 8 (Sylvester H16 = H2 (x) H8), then the exact scaling by 1/4.
 // ("Pretraining Large Language Models with NVFP4", "Random Hadamard Transforms".)
 // ---------------------------------------------------------------------------------------
-// fwht16 is the butterflies alone (no signs, no 1/4); fwht16_quarter adds the 1/4.
+// fwht16 is the butterflies alone (no signs, no 1/4); fwht16_quarter adds the 1/4. fwht16
+// runs distance 1 on scalars and distances 2, 4, 8 on packed pairs (v[2m], v[2m+1]).
 __device__ __forceinline__ void fwht16(float* v) {
 #pragma unroll
-    for (int h = 1; h < 16; h <<= 1) {
+    for (int i = 0; i < 16; i += 2) {
+        const float a = v[i], b = v[i + 1];
+        v[i] = __fadd_rn(a, b);
+        v[i + 1] = __fsub_rn(a, b);
+    }
+    uint64_t p[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if ((i & h) == 0) {
-                float a = v[i], b = v[i + h];
-                v[i] = __fadd_rn(a, b);
-                v[i + h] = __fsub_rn(a, b);
+    for (int m = 0; m < 8; ++m) p[m] = f32x2_pack(v[2 * m], v[2 * m + 1]);
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            if ((m & h) == 0) {
+                uint64_t s, d;
+                asm("add.rn.f32x2 %0, %1, %2;" : "=l"(s) : "l"(p[m]), "l"(p[m + h]));
+                asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(p[m]), "l"(p[m + h]));
+                p[m] = s;
+                p[m + h] = d;
             }
         }
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) f32x2_unpack(p[m], v[2 * m], v[2 * m + 1]);
+}
+
+// t[j] = v[j] * s for 8 values, as 4 packed multiplies
+__device__ __forceinline__ void mul8_f32x2(const float* v, float s, float* t) {
+    const uint64_t s2 = f32x2_pack(s, s);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        uint64_t q;
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q) : "l"(f32x2_pack(v[2 * m], v[2 * m + 1])), "l"(s2));
+        f32x2_unpack(q, t[2 * m], t[2 * m + 1]);
     }
 }
 __device__ __forceinline__ void fwht16_quarter(float* v) {
@@ -297,17 +335,37 @@ __device__ __forceinline__ void rht16_inplace(float* v, uint32_t signs) {
 // ---------------------------------------------------------------------------------------
 constexpr float kRht32Scale = 0.17677669529663688f;   // RN(1/sqrt(32)) = 0x3E3504F3
 
-__device__ __forceinline__ void fwht32(float (&v)[32]) {
+// Butterflies at distance 1 on scalars; distances 2..16 on packed pairs (v[2m], v[2m+1]) with
+// add/sub.rn.f32x2 (each lane of a packed op rounds like the scalar op); then a packed
+// multiply by `scale`. Results are those of the scalar stages in the same order.
+__device__ __forceinline__ void fwht32_scaled(float (&v)[32], float scale) {
 #pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
+    for (int i = 0; i < 32; i += 2) {
+        const float a = v[i], b = v[i + 1];
+        v[i] = __fadd_rn(a, b);
+        v[i + 1] = __fsub_rn(a, b);
+    }
+    uint64_t p[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if ((i & h) == 0) {
-                const float a = v[i], b = v[i + h];
-                v[i] = __fadd_rn(a, b);
-                v[i + h] = __fsub_rn(a, b);
+    for (int m = 0; m < 16; ++m) p[m] = f32x2_pack(v[2 * m], v[2 * m + 1]);
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            if ((m & h) == 0) {
+                uint64_t s, d;
+                asm("add.rn.f32x2 %0, %1, %2;" : "=l"(s) : "l"(p[m]), "l"(p[m + h]));
+                asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(p[m]), "l"(p[m + h]));
+                p[m] = s;
+                p[m + h] = d;
             }
         }
+    }
+    const uint64_t sc2 = f32x2_pack(scale, scale);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p[m]) : "l"(p[m]), "l"(sc2));
+        f32x2_unpack(p[m], v[2 * m], v[2 * m + 1]);
     }
 }
 
@@ -315,17 +373,14 @@ __device__ __forceinline__ void fwht32(float (&v)[32]) {
 __device__ __forceinline__ void rht32_forward(float (&v)[32], uint32_t signs) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(__float_as_uint(v[i]) ^ (((signs >> i) & 1u) << 31));
-    fwht32(v);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], kRht32Scale);
+    fwht32_scaled(v, kRht32Scale);
 }
 
 // inverse: butterflies, scale, signs
 __device__ __forceinline__ void rht32_inverse(float (&v)[32], uint32_t signs) {
-    fwht32(v);
+    fwht32_scaled(v, kRht32Scale);
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-        v[i] = __uint_as_float(__float_as_uint(__fmul_rn(v[i], kRht32Scale)) ^ (((signs >> i) & 1u) << 31));
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(__float_as_uint(v[i]) ^ (((signs >> i) & 1u) << 31));
 }
 
 // S2F6 block exponent (ceiling rule with the format's maximum 127/64 = 1.111111b):

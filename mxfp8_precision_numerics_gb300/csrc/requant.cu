@@ -61,8 +61,7 @@ __device__ __forceinline__ void mx_encode_block(float (&v)[32], uint64_t seed, u
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         float t[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) t[j] = __fmul_rn(v[8 * g + j], inv);
+        mul8_f32x2(v + 8 * g, inv, t);
         if (kSR) {
             // element 8g+j draws the low (j even) or high (j odd) half of word j/2
             const uint4 r = sr_block8(seed, tag, (out_idx0 >> 3) + (uint64_t)g);
@@ -171,8 +170,7 @@ __device__ __forceinline__ void mx_encode_half(float (&v)[16], bool valid, uint6
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
         float t[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) t[j] = __fmul_rn(v[8 * g + j], inv);
+        mul8_f32x2(v + 8 * g, inv, t);
         if (kSR) {
             const uint4 r = sr_block8(seed, tag, (out_idx >> 3) + (uint64_t)g);
             words[2 * g] = __byte_perm(e4m3x2_sr_hw(t[0], t[1], r.x), e4m3x2_sr_hw(t[2], t[3], r.y), 0x6420);

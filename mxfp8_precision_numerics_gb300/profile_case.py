@@ -27,6 +27,9 @@ def main():
     ap.add_argument("--N", type=int, default=4096)
     ap.add_argument("--K", type=int, default=16384)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--k", type=int, default=1, help="combine_decode: arrivals per token (M tokens)")
+    ap.add_argument("--bf16", action="store_true", help="combine: bf16 encode input / decode output")
+    ap.add_argument("--rht", action="store_true", help="quantize_mxfp4: rotate by RHT32 first")
     a = ap.parse_args()
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
@@ -52,13 +55,14 @@ def main():
         As = torch.randint(118, 136, (M, K // 32), dtype=torch.uint8, device="cuda", generator=g)
         Bs = torch.randint(118, 136, (N, K // 32), dtype=torch.uint8, device="cuda", generator=g)
         fn = lambda: F.gemm_mxfp4(A, As, B, Bs, torch.bfloat16)
-    elif a.call in ("combine_encode", "combine_decode"):
+    elif a.call == "combine_encode":
         y = torch.randn(M, K, device="cuda", generator=g)
-        codes, e8 = F.combine_encode(y, 0x9E3779B9)
-        if a.call == "combine_encode":
-            fn = lambda: F.combine_encode(y, 0x9E3779B9)
-        else:
-            fn = lambda: F.combine_decode(codes, e8, 1, 0x9E3779B9, torch.float32)
+        if a.bf16:
+            y = y.to(torch.bfloat16)
+        fn = lambda: F.combine_encode(y, 0x9E3779B9)
+    elif a.call == "combine_decode":
+        codes, e8 = F.combine_encode(torch.randn(M * a.k, K, device="cuda", generator=g), 0x9E3779B9)
+        fn = lambda: F.combine_decode(codes, e8, a.k, 0x9E3779B9, torch.bfloat16 if a.bf16 else torch.float32)
     else:
         x = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
         if a.call == "quantize_1d":
@@ -66,7 +70,7 @@ def main():
         elif a.call == "quantize_1d_rows46":
             fn = lambda: F.quantize_1d_rows(x, True)
         elif a.call == "quantize_mxfp4":
-            fn = lambda: F.quantize_mxfp4(x)
+            fn = lambda: F.quantize_mxfp4(x, a.rht, 0x5EED1234)
         elif a.call == "quantize_2d":
             fn = lambda: F.quantize_2d(x)
         elif a.call == "requant_bf16_t_rht":
