@@ -258,6 +258,26 @@ __device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
 __device__ __forceinline__ void f32x2_unpack(uint64_t d, float& lo, float& hi) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(d));
 }
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
 
 // ---------------------------------------------------------------------------------------
 // 16-point random Hadamard transform of v[0..15] in place: signs, butterflies at
@@ -281,9 +301,7 @@ __device__ __forceinline__ void fwht16(float* v) {
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             if ((m & h) == 0) {
-                uint64_t s, d;
-                asm("add.rn.f32x2 %0, %1, %2;" : "=l"(s) : "l"(p[m]), "l"(p[m + h]));
-                asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(p[m]), "l"(p[m + h]));
+                const uint64_t s = f32x2_add(p[m], p[m + h]), d = f32x2_sub(p[m], p[m + h]);
                 p[m] = s;
                 p[m + h] = d;
             }
@@ -298,9 +316,7 @@ __device__ __forceinline__ void mul8_f32x2(const float* v, float s, float* t) {
     const uint64_t s2 = f32x2_pack(s, s);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        uint64_t q;
-        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q) : "l"(f32x2_pack(v[2 * m], v[2 * m + 1])), "l"(s2));
-        f32x2_unpack(q, t[2 * m], t[2 * m + 1]);
+        f32x2_unpack(f32x2_mul(f32x2_pack(v[2 * m], v[2 * m + 1]), s2), t[2 * m], t[2 * m + 1]);
     }
 }
 __device__ __forceinline__ void fwht16_quarter(float* v) {
@@ -353,9 +369,7 @@ __device__ __forceinline__ void fwht32_scaled(float (&v)[32], float scale) {
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
             if ((m & h) == 0) {
-                uint64_t s, d;
-                asm("add.rn.f32x2 %0, %1, %2;" : "=l"(s) : "l"(p[m]), "l"(p[m + h]));
-                asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(p[m]), "l"(p[m + h]));
+                const uint64_t s = f32x2_add(p[m], p[m + h]), d = f32x2_sub(p[m], p[m + h]);
                 p[m] = s;
                 p[m + h] = d;
             }
@@ -364,8 +378,7 @@ __device__ __forceinline__ void fwht32_scaled(float (&v)[32], float scale) {
     const uint64_t sc2 = f32x2_pack(scale, scale);
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
-        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p[m]) : "l"(p[m]), "l"(sc2));
-        f32x2_unpack(p[m], v[2 * m], v[2 * m + 1]);
+        f32x2_unpack(f32x2_mul(p[m], sc2), v[2 * m], v[2 * m + 1]);
     }
 }
 

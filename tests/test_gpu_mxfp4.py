@@ -116,3 +116,33 @@ def test_mxfp4_linear_layer(F, orc):
         assert_gemm_close(y.cpu().numpy(), orc.gemm_mxfp4(oxc, oxe, owc, owe), f"MXFP4 layer rht={rht}")
         ref = (x.float() @ w.float().t()).numpy()
         assert np.linalg.norm(y.cpu().numpy() - ref) / np.linalg.norm(ref) < 0.2
+
+
+def test_mxfp4_format_comparison_full_size_sampled(F, orc):
+    """The format comparison's shape (X 16384 x 4096 with outliers, W 14336 x 4096, bf16 GEMM
+    output), in the calls the benchmark times: both quantizers checked bit for bit on sampled
+    rows (rows are independent), the GEMM's sampled output rows against the oracle's product of
+    the device's own codes (within one bf16 ulp), with and without the rotation."""
+    M, K, N = 16384, 4096, 14336
+    x = I.normal_with_outliers(M, K, seed=3)
+    w = I.normal(N, K, seed=30, std=0.02)
+    rows = np.sort(np.random.default_rng(1).choice(M, 32, replace=False))
+    rows[0], rows[-1] = 0, M - 1
+    wrows = np.sort(np.random.default_rng(2).choice(N, 32, replace=False))
+    idx = torch.from_numpy(rows).cuda()
+    for rht in (False, True):
+        xc, xe = F.quantize_mxfp4(x.cuda(), rht, SIGNS)
+        wc, we = F.quantize_mxfp4(w.cuda(), rht, SIGNS)
+        y = F.gemm_mxfp4(xc, xe, wc, we, torch.bfloat16)
+        torch.cuda.synchronize()
+        assert F.fp4q_device_status() == F.OK
+        oc, oe = orc.quantize_mxfp4(I.bf16_bits(x[rows]), rht, SIGNS)
+        assert_bytes_equal(xc[idx].cpu().numpy(), oc, f"X codes rht={rht}")
+        assert_bytes_equal(xe[idx].cpu().numpy(), oe, f"X e8m0 rht={rht}")
+        oc, oe = orc.quantize_mxfp4(I.bf16_bits(w[wrows]), rht, SIGNS)
+        widx = torch.from_numpy(wrows).cuda()
+        assert_bytes_equal(wc[widx].cpu().numpy(), oc, f"W codes rht={rht}")
+        assert_bytes_equal(we[widx].cpu().numpy(), oe, f"W e8m0 rht={rht}")
+        ref = orc.gemm_mxfp4(xc[idx].cpu().numpy(), xe[idx].cpu().numpy(), wc.cpu().numpy(), we.cpu().numpy())
+        yb = y[idx].cpu().view(torch.int16).numpy().view(np.uint16)
+        assert_bf16_rounding_of(yb, ref, f"MXFP4 16384x14336x4096 sampled rht={rht}")
