@@ -1215,32 +1215,33 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
             tc_fence_after();
             const int64_t col0 = n0 + 128 * h;
             if (kBf16Out && kEpiMode == 0) {
-                // plain bf16 output: chunks are rounded and stored as they arrive, two in flight;
-                // tensor memory goes back to the MMAs once the last two are in registers
-                uint32_t ra[32], rb[32], pk[16];
+                // plain bf16 output: all four chunks in registers before tensor memory is
+                // released (the first two rounded to bf16 pairs while the last two load), no
+                // store before the release
+                uint32_t ra[32], rb[32], p0[16], p1[16];
                 tmem_ld32_async(tacc, ra);
                 tmem_ld32_async(tacc + 32, rb);
                 tmem_wait_ld(ra);
-                pack_chunk(ra, alpha, pk);
-                tmem_ld32_async(tacc + 64, ra);
-                epi_bf16<0>(p, pk, row, row_ok, col0, amax_bits);
                 tmem_wait_ld(rb);
-                pack_chunk(rb, alpha, pk);
+                pack_chunk(ra, alpha, p0);
+                pack_chunk(rb, alpha, p1);
+                tmem_ld32_async(tacc + 64, ra);
                 tmem_ld32_async(tacc + 96, rb);
-                epi_bf16<0>(p, pk, row, row_ok, col0 + 32, amax_bits);
                 tmem_wait_ld(ra);
                 tmem_wait_ld(rb);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_leader);
-                pack_chunk(ra, alpha, pk);
-                epi_bf16<0>(p, pk, row, row_ok, col0 + 64, amax_bits);
-                pack_chunk(rb, alpha, pk);
-                epi_bf16<0>(p, pk, row, row_ok, col0 + 96, amax_bits);
+                epi_bf16<0>(p, p0, row, row_ok, col0, amax_bits);
+                epi_bf16<0>(p, p1, row, row_ok, col0 + 32, amax_bits);
+                pack_chunk(ra, alpha, p0);
+                epi_bf16<0>(p, p0, row, row_ok, col0 + 64, amax_bits);
+                pack_chunk(rb, alpha, p1);
+                epi_bf16<0>(p, p1, row, row_ok, col0 + 96, amax_bits);
             } else if (kOut < 0 ? p.d_bf16 != 0 : kBf16Out) {
-                // bf16 output with GELU or GELU backward (or chosen at run time): each 32-column chunk is rounded to bf16 pairs as soon as it is in
-                // registers (64 registers for the slice), tensor memory goes back to the MMAs,
-                // then the epilogue and the stores
+                // bf16 output with GELU or GELU backward (or chosen at run time): each 32-column
+                // chunk is rounded to bf16 pairs as soon as it is in registers (64 registers for
+                // the slice), tensor memory goes back to the MMAs, then the epilogue and the stores
                 uint32_t pk[4][16];
                 uint32_t ra[32], rb[32];
                 tmem_ld32_async(tacc, ra);
@@ -1261,22 +1262,23 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) epi_bf16<kEpiMode>(p, pk[c], row, row_ok, col0 + 32 * c, amax_bits);
             } else {
-                // fp32 output: two chunks in flight; the first two are stored while the last two
-                // load, then tensor memory goes back to the MMAs (at most 96 live registers)
+                // fp32 output: three chunks load together, the first is stored while the last
+                // loads into its registers, then tensor memory goes back to the MMAs (one chunk
+                // stored before the release; at most 96 live registers)
                 uint32_t ra[32], rb[32], rc[32];
                 tmem_ld32_async(tacc, ra);
                 tmem_ld32_async(tacc + 32, rb);
-                tmem_wait_ld(ra);
                 tmem_ld32_async(tacc + 64, rc);
-                store_chunk<kEpiMode>(p, ra, row, row_ok, col0, alpha);
-                tmem_wait_ld(rb);
-                tmem_ld32_async(tacc + 96, ra);
-                store_chunk<kEpiMode>(p, rb, row, row_ok, col0 + 32, alpha);
-                tmem_wait_ld(rc);
                 tmem_wait_ld(ra);
+                store_chunk<kEpiMode>(p, ra, row, row_ok, col0, alpha);
+                tmem_ld32_async(tacc + 96, ra);
+                tmem_wait_ld(ra);
+                tmem_wait_ld(rb);
+                tmem_wait_ld(rc);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_leader);
+                store_chunk<kEpiMode>(p, rb, row, row_ok, col0 + 32, alpha);
                 store_chunk<kEpiMode>(p, rc, row, row_ok, col0 + 64, alpha);
                 store_chunk<kEpiMode>(p, ra, row, row_ok, col0 + 96, alpha);
             }
