@@ -1480,11 +1480,13 @@ cudaError_t launch_pair_out(const GemmArgs& a, cudaStream_t st) {
 template <int kKind>
 cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
     const int out = pair_out(a.d_bf16, a.epi);
-    if constexpr (kKind == 1) {
-        // MXFP8 with a plain output measured faster as the run-time instantiation (3.09 against
-        // 2.94 PFLOP/s for bf16 at 16384 x 16384 x 4096)
-        if (out <= 1) return launch_pair_out<1, -1>(a, st);
-        if (out == 3) return launch_pair_out<1, 3>(a, st);
+    if constexpr (kKind != 0) {
+        // MXFP8 and MXFP4 with a plain output measured faster as the run-time instantiation
+        // (MXFP8 bf16 at 16384 x 16384 x 4096: 3.09 against 2.94 PFLOP/s)
+        if (out <= 1) return launch_pair_out<kKind, -1>(a, st);
+        if constexpr (kKind == 1) {
+            if (out == 3) return launch_pair_out<1, 3>(a, st);
+        }
     } else {
         if (out == 0) return launch_pair_out<kKind, 0>(a, st);
         if (out == 1) return launch_pair_out<kKind, 1>(a, st);
