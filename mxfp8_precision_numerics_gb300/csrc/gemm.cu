@@ -277,29 +277,31 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // t 2^((P(t) - z^2) log2 e), Phi(x) = 1 - erfc/2 for x >= 0 else erfc/2, phi(x) =
 // 2^(-z^2 log2 e) / sqrt(2 pi); the arithmetic on packed f32x2 pairs (each half rounds like
 // the scalar op; one instruction does two), the approximate reciprocal and exp2 scalar.
+__device__ __forceinline__ uint64_t f32x2_dup(float c) { return f32x2_pack(c, c); }
 __device__ __forceinline__ void norm_cdf_pdf2(float x0, float x1, float& c0, float& c1, float& p0, float& p1) {
     const float kLog2e = 1.4426950408889634f;
-    const uint64_t z = f32x2_mul(f32x2_pack(fabsf(x0), fabsf(x1)), f32x2_pack(0.70710678118654752f, 0.70710678118654752f));
+    const uint64_t z = f32x2_mul(f32x2_pack(fabsf(x0), fabsf(x1)), f32x2_dup(0.70710678118654752f));
     float za, zb;
-    f32x2_unpack(f32x2_fma(f32x2_pack(0.5f, 0.5f), z, f32x2_pack(1.0f, 1.0f)), za, zb);
+    f32x2_unpack(f32x2_fma(f32x2_dup(0.5f), z, f32x2_dup(1.0f)), za, zb);
     const uint64_t t = f32x2_pack(rcp_approx(za), rcp_approx(zb));
-    uint64_t q = f32x2_fma(f32x2_pack(0.22192310f, 0.22192310f), t, f32x2_pack(-0.68954533f, -0.68954533f));
-    q = f32x2_fma(q, t, f32x2_pack(0.45331991f, 0.45331991f));
-    q = f32x2_fma(q, t, f32x2_pack(0.26506487f, 0.26506487f));
-    q = f32x2_fma(q, t, f32x2_pack(1.01556778f, 1.01556778f));
-    q = f32x2_fma(q, t, f32x2_pack(-1.26633811f, -1.26633811f));
+    uint64_t q = f32x2_fma(f32x2_dup(0.22192310f), t, f32x2_dup(-0.68954533f));
+    q = f32x2_fma(q, t, f32x2_dup(0.45331991f));
+    q = f32x2_fma(q, t, f32x2_dup(0.26506487f));
+    q = f32x2_fma(q, t, f32x2_dup(1.01556778f));
+    q = f32x2_fma(q, t, f32x2_dup(-1.26633811f));
     const uint64_t zz = f32x2_mul(z, z);
     float ea, eb;
-    f32x2_unpack(f32x2_mul(f32x2_sub(q, zz), f32x2_pack(kLog2e, kLog2e)), ea, eb);
+    f32x2_unpack(f32x2_mul(f32x2_sub(q, zz), f32x2_dup(kLog2e)), ea, eb);
     const uint64_t erfc_z = f32x2_mul(t, f32x2_pack(ex2_approx(ea), ex2_approx(eb)));
     float ca, cb, ha, hb;
-    f32x2_unpack(f32x2_fma(f32x2_pack(-0.5f, -0.5f), erfc_z, f32x2_pack(1.0f, 1.0f)), ca, cb);
-    f32x2_unpack(f32x2_mul(f32x2_pack(0.5f, 0.5f), erfc_z), ha, hb);
+    f32x2_unpack(f32x2_fma(f32x2_dup(-0.5f), erfc_z, f32x2_dup(1.0f)), ca, cb);
+    f32x2_unpack(f32x2_mul(f32x2_dup(0.5f), erfc_z), ha, hb);
     c0 = x0 >= 0.0f ? ca : ha;
     c1 = x1 >= 0.0f ? cb : hb;
     float fa, fb;
-    f32x2_unpack(f32x2_mul(zz, f32x2_pack(-kLog2e, -kLog2e)), fa, fb);
-    f32x2_unpack(f32x2_mul(f32x2_pack(ex2_approx(fa), ex2_approx(fb)), f32x2_pack(0.39894228040143268f, 0.39894228040143268f)), p0, p1);
+    f32x2_unpack(f32x2_mul(zz, f32x2_dup(-kLog2e)), fa, fb);
+    const uint64_t e2 = f32x2_pack(ex2_approx(fa), ex2_approx(fb));
+    f32x2_unpack(f32x2_mul(e2, f32x2_dup(0.39894228040143268f)), p0, p1);   // e^(-x^2/2) / sqrt(2 pi)
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
@@ -347,7 +349,8 @@ __device__ __forceinline__ void epi_bf16(const Params& p, const uint32_t (&pk)[1
                 const float h0 = __uint_as_float(hw[i] << 16), h1 = __uint_as_float(hw[i] & 0xFFFF0000u);
                 float c0, c1, p0, p1;
                 norm_cdf_pdf2(h0, h1, c0, c1, p0, p1);
-                const uint64_t gr = f32x2_fma(f32x2_pack(h0, h1), f32x2_pack(p0, p1), f32x2_pack(c0, c1));   // GELU'(h)
+                // GELU'(h) = Phi(h) + h phi(h)
+                const uint64_t gr = f32x2_fma(f32x2_pack(h0, h1), f32x2_pack(p0, p1), f32x2_pack(c0, c1));
                 float o0, o1;
                 f32x2_unpack(f32x2_mul(f32x2_pack(g0, g1), gr), o0, o1);
                 o[i] = pack_bf16x2(o0, o1);
