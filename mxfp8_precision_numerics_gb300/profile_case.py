@@ -20,7 +20,8 @@ def _e4m3(shape, g):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--call", required=True,
-                    choices=["gemm_mxfp8", "gemm_nvfp4", "gemm_nvfp4_gelu", "gemm_mxfp4", "quantize_1d", "quantize_2d",
+                    choices=["gemm_mxfp8", "gemm_mxfp8_dgelu", "gemm_nvfp4", "gemm_nvfp4_gelu", "gemm_mxfp4", "quantize_1d",
+                             "quantize_2d",
                              "quantize_1d_rows46", "quantize_mxfp4", "requant_bf16_t_rht", "requant_bf16_rows",
                              "requant_nvfp4_t_rht", "requant_nvfp4_2d_t", "combine_encode", "combine_decode"])
     ap.add_argument("--M", type=int, default=8192)
@@ -39,6 +40,12 @@ def main():
         As = torch.randint(120, 134, (M, K // 32), dtype=torch.uint8, device="cuda", generator=g)
         Bs = torch.randint(120, 134, (N, K // 32), dtype=torch.uint8, device="cuda", generator=g)
         fn = lambda: F.gemm_mxfp8(A, As, B, Bs, torch.bfloat16)
+    elif a.call == "gemm_mxfp8_dgelu":
+        A, B = _e4m3((M, K), g), _e4m3((N, K), g)
+        As = torch.randint(120, 134, (M, K // 32), dtype=torch.uint8, device="cuda", generator=g)
+        Bs = torch.randint(120, 134, (N, K // 32), dtype=torch.uint8, device="cuda", generator=g)
+        H = torch.randn(M, N, device="cuda", generator=g).to(torch.bfloat16)
+        fn = lambda: F.gemm_mxfp8_dgelu(A, As, B, Bs, H)
     elif a.call in ("gemm_nvfp4", "gemm_nvfp4_gelu"):
         A = torch.randint(0, 256, (M, K // 2), dtype=torch.uint8, device="cuda", generator=g)
         B = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda", generator=g)
