@@ -149,7 +149,8 @@ FP4Q_API int fp4q_quantize_2d(const void* w_bf16, int64_t rows, int64_t cols, in
  * fp4q_quantize_2d computing its own amax.
  *   batch > FP4Q_NOALLOC_MAX_BATCH is rejected with FP4Q_ERR_SHAPE before any launch.
  *   The first call on a device looks up the array's device address (once per device, with
- *   that device current); make that first call before any stream capture.
+ *   that device current, and again after the device's context changes, e.g. after a
+ *   cudaDeviceReset); make that first call before any stream capture.
  *   Every call on a device shares the array: calls whose work may overlap on the GPU (two
  *   streams without ordering between them) race on it. Calls ordered on one stream are safe;
  *   each call clears the part it uses before accumulating the amax.
@@ -379,6 +380,24 @@ FP4Q_API int fp4q_gemm_nvfp4_combine(const uint8_t* a, const uint8_t* a_scales, 
  * This is the only call that blocks the host.
  */
 FP4Q_API int fp4q_device_status(fp4q_stream_t stream);
+
+/*
+ * fp4q_test_gemm_wait_timeout — failure-detection test of the bounded waits. The pages have no
+ * counterpart: it exercises the library's own failure path without faulting the GPU.
+ * Launches the CTA-pair MXFP8 GEMM kernel of fp4q_gemm_mxfp8 (fp32 output) on the given
+ * operands with its producers issuing no copies, so no pipeline barrier ever completes: every
+ * mbarrier wait of the kernel gives up after wait_limit_ns, raises the device error word and
+ * ends its role; the kernel frees its tensor memory and returns with no copy in flight. d is
+ * left unwritten. The next fp4q_device_status on the stream returns FP4Q_ERR_TIMEOUT (and
+ * clears the word); later calls run normally.
+ *   wait_limit_ns in [1e6, 2e9] (else FP4Q_ERR_ARG); the kernel takes a few limits in all.
+ *   Shapes as fp4q_gemm_mxfp8 with M > 128 and K % 512 == 0 (the pair kernel's), 16-byte
+ *   aligned pointers; a, a_scales, b, b_scales and d must be valid device buffers of those
+ *   shapes (their tensor maps are built as for a real GEMM; nothing is read or written).
+ */
+FP4Q_API int fp4q_test_gemm_wait_timeout(const uint8_t* a, const uint8_t* a_scales,
+                    const uint8_t* b, const uint8_t* b_scales, void* d,
+                    int64_t M, int64_t N, int64_t K, int64_t wait_limit_ns, fp4q_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -25,15 +25,6 @@ int num_sms() {
 // tie of the grid, on saturation and on a dense sweep; the ALU rule stays as the reference.
 bool use_hw_e2m1() { return true; }
 
-}  // namespace fp4q
-
-namespace {
-
-inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
-
-inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA; }
-
 // The kernels use tcgen05 / TMA instructions of compute capability 10.x.
 int check_device() {
     static int cached_dev = -1, cached = FP4Q_OK;
@@ -48,6 +39,18 @@ int check_device() {
     }
     return cached;
 }
+
+}  // namespace fp4q
+
+namespace {
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA; }
+
+using fp4q::check_device;
+
 
 }  // namespace
 
@@ -350,6 +353,38 @@ int fp4q_gemm_mxfp8(const uint8_t* a, const uint8_t* a_scales,
     g.K = K;
     g.groups = 1;
     g.group_offsets = nullptr;
+    return cuda_status(fp4q::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp4q_test_gemm_wait_timeout(const uint8_t* a, const uint8_t* a_scales,
+                                const uint8_t* b, const uint8_t* b_scales, void* d,
+                                int64_t M, int64_t N, int64_t K, int64_t wait_limit_ns,
+                                fp4q_stream_t stream) {
+    if (!a || !a_scales || !b || !b_scales || !d) return FP4Q_ERR_NULL;
+    if (wait_limit_ns < 1000000 || wait_limit_ns > 2000000000) return FP4Q_ERR_ARG;
+    // the CTA-pair kernel's shapes: more than one 128-row tile, whole scale units of 4 K-blocks
+    if (M <= 128 || N < 16 || N % 16 != 0 || K < 512 || K % 512 != 0) return FP4Q_ERR_SHAPE;
+    if (M > 2147483647 || N > 2147483647) return FP4Q_ERR_SHAPE;
+    if (!al16(a) || !al16(b) || !al16(a_scales) || !al16(b_scales) || !al16(d)) return FP4Q_ERR_ALIGN;
+    if (int dv = check_device()) return dv;
+    fp4q::GemmArgs g;
+    g.kind = 1;
+    g.a = a;
+    g.a_scales = a_scales;
+    g.a_s_dec = nullptr;
+    g.b = b;
+    g.b_scales = b_scales;
+    g.b_scale_kind = 1;
+    g.b_s_dec = nullptr;
+    g.d = d;
+    g.d_bf16 = 0;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.groups = 1;
+    g.group_offsets = nullptr;
+    g.wait_limit_ns = wait_limit_ns;
+    g.no_copies = 1;
     return cuda_status(fp4q::launch_gemm(g, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -6,6 +6,7 @@
 namespace fp4q {
 
 int num_sms();            // SM count of the current device (cached per device)
+int check_device();       // FP4Q_OK on a compute-capability 10.x device (cached per device)
 bool use_hw_e2m1();       // convert E2M1 with the hardware cvt (shown equal to the ALU rule)
 
 cudaError_t launch_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int64_t batch,
@@ -68,6 +69,11 @@ struct GemmArgs {
     float* amax_out = nullptr;   // epi 1; may be NULL
     uint32_t rht32_signs = 0;    // epi 3: combine encode (d = S2F6 bytes, d2 = E8M0 per 32), fp32 path
     int a_sdec_rows = 0;         // NVFP4: A carries one outer scale per row
+    // failure-detection test (CTA-pair kernel only): every mbarrier wait gives up after
+    // wait_limit_ns (0: the default 1.5 s), and with no_copies the producers issue no copies,
+    // so the waits run out, the kernel raises the device error word and returns
+    int64_t wait_limit_ns = 0;
+    int no_copies = 0;
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st);
 int read_and_clear_device_error(cudaStream_t st, int* flag);

@@ -103,6 +103,8 @@ struct Params {
     void* d2;
     const uint16_t* aux;
     float* amax_out;
+    uint64_t wait_ns;          // pair kernel: the limit of every mbarrier wait
+    int no_copies;             // pair kernel, failure-detection test: the producers issue no copies
 };
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -131,12 +133,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 // Bounded wait on the phase with the given parity. false = gave up (error word raised).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kTimeoutNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && globaltimer() - t0 > kTimeoutNs) {
+        if ((it & 255u) == 0 && globaltimer() - t0 > limit_ns) {
             atomicOr(&g_device_error, 1u);
             return false;
         }
@@ -542,12 +544,12 @@ __device__ __forceinline__ bool mbar_try_wait_pair(uint64_t* bar, uint32_t parit
     return ok != 0;
 }
 // bounded wait on a barrier that also receives arrivals from the peer CTA
-__device__ __forceinline__ bool mbar_wait_pair(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_pair(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kTimeoutNs) {
     if (mbar_try_wait_pair(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_pair(bar, parity)) return true;
-        if ((it & 255u) == 0 && globaltimer() - t0 > kTimeoutNs) {
+        if ((it & 255u) == 0 && globaltimer() - t0 > limit_ns) {
             atomicOr(&g_device_error, 1u);
             return false;
         }
@@ -564,12 +566,12 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
                  : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"((uint32_t)FP4Q_IDLE_SUSPEND_NS) : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kTimeoutNs) {
     const uint64_t t0 = globaltimer();
     for (;;) {
         if (FP4Q_IDLE_SUSPEND_NS > 0 ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait_pair(bar, parity))
             return true;
-        if (globaltimer() - t0 > kTimeoutNs) {
+        if (globaltimer() - t0 > limit_ns) {
             atomicOr(&g_device_error, 1u);
             return false;
         }
@@ -1009,6 +1011,7 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tmem_empty + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint64_t wl = p.wait_ns;
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
     const int cid = (int)(blockIdx.x >> 1), ncl = (int)(gridDim.x >> 1);
@@ -1064,8 +1067,8 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         // previous unit
         auto load_next_sf = [&]() -> bool {
             const int r = sf_u % R;
-            if (!mbar_wait(&sf_empty[r], ((uint32_t)(sf_u / R) & 1u) ^ 1u)) return false;
-            if (lane == 0) {
+            if (!mbar_wait(&sf_empty[r], ((uint32_t)(sf_u / R) & 1u) ^ 1u, wl)) return false;
+            if (lane == 0 && !p.no_copies) {
                 uint8_t* dst = sf_stage + r * kSfUnit;
                 mbar_arrive_expect_tx(&sf_full[r], kSfUnitA + (p.b_sc_2d ? 16u : (uint32_t)kBN) * kW);
                 tma_load_2d(&p.tma_sfa, &sf_full[r], dst, sf_uk * (int)kW, (int32_t)sf_m0);
@@ -1091,9 +1094,9 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
             while (ok && sf_u < total_units && sf_u <= gk / G + DU) ok = load_next_sf();
             if (!ok) break;
             const int s = gk % S;
-            if (!mbar_wait_pair(&empty[s], ((uint32_t)(gk / S) & 1u) ^ 1u)) break;
+            if (!mbar_wait_pair(&empty[s], ((uint32_t)(gk / S) & 1u) ^ 1u, wl)) break;
             uint8_t* st = smem + s * kPairStage;
-            if (lane == 0) {
+            if (lane == 0 && !p.no_copies) {
                 if (leader) mbar_arrive_expect_tx(&full[s], 2 * kPairStage);
                 const uint32_t bar = leader_addr(&full[s]);
                 tma_load_2d_pair_hint(&p.tma_a, bar, st, kb * kBKBytes, (int32_t)m0, pol_a);
@@ -1108,23 +1111,25 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         // Every copy this CTA issued has landed before it may exit (on an early exit the
         // consumers no longer wait for them). The leader's `full` counts both CTAs' A/B
         // bytes; the follower is held at the final cluster barrier until the leader is done.
+        // (The failure-detection test mode issued none.)
+        if (p.no_copies) issued = sf_u = 0;
         if (leader)
             for (int gk = issued > S ? issued - S : 0; gk < issued; ++gk)
-                mbar_wait_pair(&full[gk % S], (uint32_t)(gk / S) & 1u);
-        for (int u = sf_u > R ? sf_u - R : 0; u < sf_u; ++u) mbar_wait(&sf_full[u % R], (uint32_t)(u / R) & 1u);
+                mbar_wait_pair(&full[gk % S], (uint32_t)(gk / S) & 1u, wl);
+        for (int u = sf_u > R ? sf_u - R : 0; u < sf_u; ++u) mbar_wait(&sf_full[u % R], (uint32_t)(u / R) & 1u, wl);
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer (leader only)
         if (leader && lane == 0) {
             bool ok = true;
             for (int ti = 0; ti < my_tiles && ok; ++ti) {
                 // the epilogue has copied the previous tile's accumulator out of tensor memory
-                if (!mbar_wait_pair(tmem_empty, ((uint32_t)ti & 1u) ^ 1u)) break;
+                if (!mbar_wait_pair(tmem_empty, ((uint32_t)ti & 1u) ^ 1u, wl)) break;
                 tc_fence_after();
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     const int gk = ti * p.num_kb + kb;
                     const int s = gk % S, t = gk % T;
-                    if (!mbar_wait_pair(&full[s], (uint32_t)(gk / S) & 1u) ||
-                        !mbar_wait_pair(&sf_ready[t], (uint32_t)(gk / T) & 1u)) {
+                    if (!mbar_wait_pair(&full[s], (uint32_t)(gk / S) & 1u, wl) ||
+                        !mbar_wait_pair(&sf_ready[t], (uint32_t)(gk / T) & 1u, wl)) {
                         ok = false;
                         break;
                     }
@@ -1170,9 +1175,9 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         static_assert(G % 2 == 0, "writer passes take K-blocks in pairs");
         for (int gk = 0; gk < total_kb; gk += 2) {
             const int u = gk / G, r = u % R, t0 = gk % T, t1 = (gk + 1) % T;
-            if (!mbar_wait(&sf_full[r], (uint32_t)(u / R) & 1u)) break;
-            if (!mbar_wait_pair(T == S ? &empty[t0] : &sf_free[t0], ((uint32_t)(gk / T) & 1u) ^ 1u)) break;
-            if (!mbar_wait_pair(T == S ? &empty[t1] : &sf_free[t1], ((uint32_t)((gk + 1) / T) & 1u) ^ 1u)) break;
+            if (!mbar_wait(&sf_full[r], (uint32_t)(u / R) & 1u, wl)) break;
+            if (!mbar_wait_pair(T == S ? &empty[t0] : &sf_free[t0], ((uint32_t)(gk / T) & 1u) ^ 1u, wl)) break;
+            if (!mbar_wait_pair(T == S ? &empty[t1] : &sf_free[t1], ((uint32_t)((gk + 1) / T) & 1u) ^ 1u, wl)) break;
             tc_fence_after();
             write_unit_scales<kKind>(sf_stage + r * kSfUnit, gk % G, p.b_sc_2d != 0,
                                      tmem + lane_base + kSfCol + (uint32_t)t0 * kSfCols, lane, warp);
@@ -1214,7 +1219,7 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
             }
             // per-row outer scale of A: loaded before the wait for the accumulator
             const float alpha = rows_sd ? (row_ok ? __fmul_rn(p.a_s_dec[row], b_sd) : 0.0f) : alpha_t;
-            if (!mbar_wait_idle(accum_full, (uint32_t)ti & 1u)) break;
+            if (!mbar_wait_idle(accum_full, (uint32_t)ti & 1u, wl)) break;
             tc_fence_after();
             const int64_t col0 = n0 + 128 * h;
             if (kBf16Out && kEpiMode == 0) {
@@ -1445,6 +1450,8 @@ cudaError_t launch_pair_out(const GemmArgs& a, cudaStream_t st) {
     p.num_kb = (int)(a.K / Cfg<kKind>::kValuesPerStage);
     p.n_tiles = (int)((a.N + kBN - 1) / kBN);
     p.groups = a.groups;
+    p.wait_ns = a.wait_limit_ns > 0 ? (uint64_t)a.wait_limit_ns : kTimeoutNs;
+    p.no_copies = a.no_copies;
     int64_t tiles_m = 0;
     for (int gi = 0; gi < a.groups; ++gi) {
         const int64_t lo = a.groups == 1 ? 0 : a.group_offsets[gi];
@@ -1525,6 +1532,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t st) {
     const int64_t g_units = a.kind == 0 ? Pair<0>::G : Pair<1>::G;
     const bool sf_tma = sc_ld % 16 == 0 && stages % g_units == 0 &&
                         ((reinterpret_cast<uintptr_t>(a.a_scales) | reinterpret_cast<uintptr_t>(a.b_scales)) & 15u) == 0;
+    if (a.no_copies && !(sf_tma && a.M > 128)) return cudaErrorInvalidValue;   // the test mode is the pair kernel's
     if (FP4Q_GEMM_PAIR && (a.groups > 1 || a.M > 128) && stages >= FP4Q_PAIR_MIN_STAGES && sf_tma)
         return a.kind == 0 ? launch_pair<0>(a, st) : launch_pair<1>(a, st);
     return a.kind == 0 ? launch_kind<0>(a, st) : launch_kind<1>(a, st);

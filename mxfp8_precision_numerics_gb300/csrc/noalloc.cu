@@ -26,19 +26,41 @@ static __device__ __align__(256) float g_noalloc_amax[FP4Q_NOALLOC_MAX_BATCH];
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 float* g_scratch_addr[kMaxDevices] = {nullptr};
+void* g_scratch_ctx[kMaxDevices] = {nullptr};
 
-// The device address of the array for the current device, looked up once per device (with
-// that device current). In host code the array's name is only a host-side stand-in, so the
-// kernels must be given this address.
+// The current context of the calling thread (driver entry point, looked up once), or NULL.
+void* current_context() {
+    typedef int (*CtxGetCurrentFn)(void**);
+    static CtxGetCurrentFn fn = nullptr;
+    static bool looked_up = false;
+    if (!looked_up) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(f);
+        looked_up = true;
+    }
+    void* ctx = nullptr;
+    if (fn && fn(&ctx) != 0) ctx = nullptr;
+    return ctx;
+}
+
+// The device address of the array for the current device, looked up with that device current
+// the first time it is used and again whenever the device's context has changed since (after a
+// cudaDeviceReset the module is loaded anew and the array may sit elsewhere). In host code the
+// array's name is only a host-side stand-in, so the kernels must be given this address.
 int scratch_for_current_device(float** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FP4Q_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return FP4Q_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[dev]) {
+    void* ctx = current_context();
+    if (!g_scratch_addr[dev] || ctx != g_scratch_ctx[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_amax) != cudaSuccess || !p) return FP4Q_ERR_CUDA;
         g_scratch_addr[dev] = static_cast<float*>(p);
+        g_scratch_ctx[dev] = current_context();   // the lookup may have made the primary context current
     }
     *out = g_scratch_addr[dev];
     return FP4Q_OK;
@@ -58,11 +80,7 @@ extern "C" int fp4q_quantize_2d_noalloc(const void* w_bf16, int64_t rows, int64_
     if (batch > 1 && batch_stride < rows * ld) return FP4Q_ERR_SHAPE;
     if (rows / 16 > 65535) return FP4Q_ERR_SHAPE;
     if (!al16(w_bf16) || ld % 8 != 0 || batch_stride % 8 != 0 || !al16(codes)) return FP4Q_ERR_ALIGN;
-    int major = 0, dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
-        return FP4Q_ERR_CUDA;
-    if (major != 10) return FP4Q_ERR_UNSUPPORTED;
+    if (int dv = fp4q::check_device()) return dv;
     float* amax = nullptr;
     if (int s = scratch_for_current_device(&amax)) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -67,6 +67,7 @@ _SIGS = {
     "fp4q_gemm_nvfp4_combine": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _u32, _vp, _vp, _i64, _i64, _i64,
                                        _int, _vp, _vp]),
     "fp4q_device_status": (_int, [_vp]),
+    "fp4q_test_gemm_wait_timeout": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -224,6 +225,13 @@ def fp4q_gemm_nvfp4_combine(a, a_scales, a_s_dec, b, b_scales, b_scale_kind, b_s
 
 def fp4q_device_status(stream=None):
     return _lib.fp4q_device_status(_stream(stream))
+
+
+def fp4q_test_gemm_wait_timeout(a, a_scales, b, b_scales, d, M, N, K, wait_limit_ns, stream=None):
+    """The failure-detection test launch (returns the launch status; fp4q_device_status then
+    reports FP4Q_ERR_TIMEOUT)."""
+    return _lib.fp4q_test_gemm_wait_timeout(_ptr(a), _ptr(a_scales), _ptr(b), _ptr(b_scales), _ptr(d), M, N, K,
+                                            int(wait_limit_ns), _stream(stream))
 
 
 # ------------------------------------------------------------------ allocating helpers

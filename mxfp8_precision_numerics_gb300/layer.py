@@ -104,8 +104,82 @@ def mlp_backward(dy, saved, seed, rht_signs, stream=None):
     # layer 2's dgrad GEMM applies GELU'(h): dh = (dy w2) * GELU'(h)
     dh, dw2 = linear_backward(dy, s2, seed, rht_signs, stream=stream, dgelu_h=h)
     # a second layer draws from its own counter stream: offset the seed
-    dx, dw1 = linear_backward(dh, s1, seed ^ 0x9E3779B97F4A7C15, rht_signs, stream=stream)
+    dx, dw1 = linear_backward(dh, s1, seed ^ SEED2_OFFSET, rht_signs, stream=stream)
     return dx, dw1, dw2
+
+
+SEED2_OFFSET = 0x9E3779B97F4A7C15   # the second layer's counter stream: seed ^ this
+
+
+def _direct(kind, units, fn, *a, **k):
+    return fn(*a, **k)
+
+
+def mlp_step(x, w1, w2, dy, seed, rht_signs, outer="tensor", call=None):
+    """One forward + backward of the GPT MLP block, call by call, returning every stage's
+    output in a dict (the same calls as mlp_forward + mlp_backward, with the intermediates
+    kept so that each can be checked on its own input).
+
+    x [M, D], w1 [Fh, D], w2 [D, Fh], dy [M, D], all bf16. outer: "tensor" or "row" (the
+    activations x and GELU(h) per token row with 4/6 block scales). call(kind, units, fn,
+    *args, **kwargs) runs each library call (default: directly); kind names the call's class
+    and units its algorithmic size: elements for the HBM-bound calls, FLOPs for the GEMMs.
+    """
+    C = call or _direct
+    M, D = x.shape
+    Fh = w1.shape[0]
+    rows = outer == "row"
+    x_kind = F.IN_NVFP4_1D_ROWS if rows else F.IN_NVFP4_1D
+    S = {}
+    # ---- forward
+    if rows:
+        S["xq"] = C("quantize_1d_rows46", M * D, F.quantize_1d_rows, x, True)
+    else:
+        xc, xs, xsd, xa = C("quantize_1d", M * D, F.quantize_1d, x)
+        S["xq"], S["x_amax"] = (xc, xs, xsd), xa
+    w1c, w1s, w1d, w1a = C("quantize_2d", Fh * D, F.quantize_2d, w1)
+    S["w1q"], S["w1_amax"] = (w1c, w1s, w1d), w1a
+    xc, xs, xsd = S["xq"]
+    # layer 1 with GELU in its epilogue: h, a = GELU(h) (and max|a|, layer 2's quantize amax)
+    if rows:
+        S["h"], S["a"] = C("gemm_nvfp4", 2.0 * M * Fh * D, F.gemm_nvfp4_gelu_rows, xc, xs, xsd, w1c, w1s,
+                           F.SCALE_2D, w1d)
+        S["aq"] = C("quantize_1d_rows46", M * Fh, F.quantize_1d_rows, S["a"], True)
+    else:
+        S["h"], S["a"], S["a_amax"] = C("gemm_nvfp4", 2.0 * M * Fh * D, F.gemm_nvfp4_gelu, xc, xs, xsd, w1c, w1s,
+                                        F.SCALE_2D, w1d)
+        ac, as_, ad, _ = C("quantize_1d_given_amax", M * Fh, F.quantize_1d, S["a"], amax_in=S["a_amax"])
+        S["aq"] = (ac, as_, ad)
+    w2c, w2s, w2d, w2a = C("quantize_2d", D * Fh, F.quantize_2d, w2)
+    S["w2q"], S["w2_amax"] = (w2c, w2s, w2d), w2a
+    ac, as_, ad = S["aq"]
+    gemm2 = F.gemm_nvfp4_rows if rows else F.gemm_nvfp4
+    S["y"] = C("gemm_nvfp4", 2.0 * M * D * Fh, gemm2, ac, as_, ad, w2c, w2s, F.SCALE_2D, w2d, torch.bfloat16)
+    # ---- backward, layer 2: dA = dY W2 (times GELU'(h) in the epilogue), dW2 = dY^T A_q
+    sr = F.SR
+    S["g"] = C("requant_bf16", M * D, F.requant_mxfp8, F.IN_BF16, dy, None, None, M, D, 0, 0, 0, sr, seed,
+               F.TAG_DY_ROWS)
+    S["w2t"] = C("requant_nvfp4_2d", D * Fh, F.requant_mxfp8, F.IN_NVFP4_2D, w2c, w2s, w2d, D, Fh, 1, 0, 0, sr,
+                 seed, F.TAG_WT)
+    S["dh"] = C("gemm_mxfp8", 2.0 * M * Fh * D, F.gemm_mxfp8_dgelu, *S["g"], *S["w2t"], S["h"])
+    S["gt"] = C("requant_bf16", M * D, F.requant_mxfp8, F.IN_BF16, dy, None, None, M, D, 1, 1, rht_signs, sr,
+                seed, F.TAG_DY_T)
+    S["at"] = C("requant_nvfp4_1d", M * Fh, F.requant_mxfp8, x_kind, ac, as_, ad, M, Fh, 1, 1, rht_signs, sr,
+                seed, F.TAG_XT)
+    S["dw2"] = C("gemm_mxfp8", 2.0 * D * Fh * M, F.gemm_mxfp8, *S["gt"], *S["at"], torch.float32)
+    # ---- backward, layer 1: dX = dH W1, dW1 = dH^T X_q (its own counter stream)
+    seed2 = seed ^ SEED2_OFFSET
+    S["g1"] = C("requant_bf16", M * Fh, F.requant_mxfp8, F.IN_BF16, S["dh"], None, None, M, Fh, 0, 0, 0, sr,
+                seed2, F.TAG_DY_ROWS)
+    S["w1t"] = C("requant_nvfp4_2d", Fh * D, F.requant_mxfp8, F.IN_NVFP4_2D, w1c, w1s, w1d, Fh, D, 1, 0, 0, sr,
+                 seed2, F.TAG_WT)
+    S["dx"] = C("gemm_mxfp8", 2.0 * M * D * Fh, F.gemm_mxfp8, *S["g1"], *S["w1t"], torch.bfloat16)
+    S["g1t"] = C("requant_bf16", M * Fh, F.requant_mxfp8, F.IN_BF16, S["dh"], None, None, M, Fh, 1, 1,
+                 rht_signs, sr, seed2, F.TAG_DY_T)
+    S["xt"] = C("requant_nvfp4_1d", M * D, F.requant_mxfp8, x_kind, xc, xs, xsd, M, D, 1, 1, rht_signs, sr,
+                seed2, F.TAG_XT)
+    S["dw1"] = C("gemm_mxfp8", 2.0 * Fh * D * M, F.gemm_mxfp8, *S["g1t"], *S["xt"], torch.float32)
+    return S
 
 
 def mlp_gemm_flops(M, D, Fh):

@@ -25,7 +25,7 @@
  *   Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
  *         1, 2, 3", SC'11, section 4 (Philox round function and key schedule).
  *
- * Readings where the pages are silent or disagree (each also listed in the design doc):
+ * Readings where the pages are silent or disagree:
  *   - E2M1 ties go to the even code (round-to-nearest-even, [NV] step 4); a value
  *     that rounds to zero keeps its sign ([VZ] §6 round_float uses copysign).
  *   - The scale arithmetic follows [NV] steps 1-4 literally in fp32:
@@ -732,4 +732,43 @@ EXPORT void orc_dequant_mxfp4(const uint8_t* codes, const uint8_t* e8m0, int64_t
         for (int64_t c = 0; c < cols; ++c)
             out[r * cols + c] = orc_e2m1_decode(get_code(codes, cols / 2, r, c))
                                 * ldexp(1.0, (int)e8m0[r * (cols / 32) + c / 32] - 127);
+}
+
+/* ------------------------------------------------------------------------- */
+/* GELU between the MLP's two linear layers                                   */
+/* ------------------------------------------------------------------------- */
+/* 4bit.vizuara.ai §13-14 puts GELU between the two NVFP4 linear layers of the MLP
+ * block. The exact-erf GELU (Hendrycks and Gimpel, "Gaussian Error Linear Units",
+ * 2016, §2): GELU(x) = x * Phi(x), Phi the standard normal cdf, and its derivative
+ * GELU'(x) = Phi(x) + x * phi(x), phi the standard normal density. Phi is written
+ * through the complementary error function, Phi(x) = erfc(-x / sqrt 2) / 2, which
+ * loses nothing in the lower tail (1 + erf(x / sqrt 2) cancels for x < -4). Double
+ * precision throughout; libm's erfc and exp are the library steps. */
+EXPORT double orc_normal_cdf(double x)
+{
+    return 0.5 * erfc(-x / sqrt(2.0));
+}
+
+EXPORT double orc_normal_pdf(double x)
+{
+    return exp(-0.5 * x * x) / sqrt(2.0 * 3.14159265358979323846);
+}
+
+EXPORT double orc_gelu(double x)
+{
+    return x * orc_normal_cdf(x);
+}
+
+EXPORT double orc_gelu_grad(double x)
+{
+    return orc_normal_cdf(x) + x * orc_normal_pdf(x);
+}
+
+/* GELU (grad == 0) or GELU' (grad != 0) of n bf16 values, in double. */
+EXPORT void orc_gelu_bf16(const uint16_t* h, int64_t n, int grad, double* out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        const double x = (double)bf16_value(h[i]);
+        out[i] = grad ? orc_gelu_grad(x) : orc_gelu(x);
+    }
 }

@@ -110,6 +110,11 @@ def lib():
         L.orc_quantize_mxfp4.argtypes = [_u16p, _i64, _i64, _i64, ctypes.c_int, ctypes.c_uint32, _u8p, _u8p]
         L.orc_dequant_mxfp4.restype = None
         L.orc_dequant_mxfp4.argtypes = [_u8p, _u8p, _i64, _i64, _f64p]
+        for fn in (L.orc_normal_cdf, L.orc_normal_pdf, L.orc_gelu, L.orc_gelu_grad):
+            fn.restype = ctypes.c_double
+            fn.argtypes = [ctypes.c_double]
+        L.orc_gelu_bf16.restype = None
+        L.orc_gelu_bf16.argtypes = [_u16p, _i64, ctypes.c_int, _f64p]
         _LIB = L
     return _LIB
 
@@ -395,29 +400,65 @@ def dequant_mxfp4(codes, e8m0):
     return out
 
 
-def gemm_mxfp4(a_codes, a_e8m0, b_codes, b_e8m0):
+def gemm_mxfp4(a_codes, a_e8m0, b_codes, b_e8m0, with_abs=False):
     """D = A . B^T on exactly dequantized MXFP4 operands, float64."""
-    return dequant_mxfp4(a_codes, a_e8m0) @ dequant_mxfp4(b_codes, b_e8m0).T
+    return _product(dequant_mxfp4(a_codes, a_e8m0), dequant_mxfp4(b_codes, b_e8m0), with_abs)
+
+
+# ---------------------------------------------------------------- GELU
+def normal_cdf(x):
+    return lib().orc_normal_cdf(float(x))
+
+
+def normal_pdf(x):
+    return lib().orc_normal_pdf(float(x))
+
+
+def gelu(x):
+    """GELU(x) = x Phi(x) (exact-erf form), float64."""
+    return lib().orc_gelu(float(x))
+
+
+def gelu_grad(x):
+    """GELU'(x) = Phi(x) + x phi(x), float64."""
+    return lib().orc_gelu_grad(float(x))
+
+
+def gelu_bf16(h_bits, grad=False):
+    """GELU (or GELU') of bf16 bit patterns, float64, same shape."""
+    h = _c(h_bits, np.uint16)
+    out = np.empty(h.shape, np.float64)
+    lib().orc_gelu_bf16(_p(h, _u16p), h.size, 1 if grad else 0, _p(out, _f64p))
+    return out
 
 
 # ---------------------------------------------------------------- GEMMs
-def gemm_nvfp4(a_codes, a_scales, a_kind, a_sdec, b_codes, b_scales, b_kind, b_sdec):
+# Each GEMM reference returns D = A . B^T on exactly dequantized operands (float64). With
+# with_abs=True it returns (D, |A| . |B|^T, K): also the sum of |a_k b_k| behind every output
+# element (the scale of the rounding error an fp32 accumulation of that element can carry)
+# and the contraction length.
+def _product(A, B, with_abs):
+    D = A @ B.T
+    return (D, np.abs(A) @ np.abs(B).T, A.shape[1]) if with_abs else D
+
+
+def gemm_nvfp4(a_codes, a_scales, a_kind, a_sdec, b_codes, b_scales, b_kind, b_sdec, with_abs=False):
     """D = A . B^T on exactly dequantized NVFP4 operands, float64."""
     A = dequant_nvfp4(a_codes, a_scales, a_kind, a_sdec)
     B = dequant_nvfp4(b_codes, b_scales, b_kind, b_sdec)
-    return A @ B.T
+    return _product(A, B, with_abs)
 
 
-def gemm_nvfp4_rows(a_codes, a_scales, a_sdec_rows, b_codes, b_scales, b_kind, b_sdec):
+def gemm_nvfp4_rows(a_codes, a_scales, a_sdec_rows, b_codes, b_scales, b_kind, b_sdec, with_abs=False):
     """D = A . B^T with A carrying a per-row outer scale, float64."""
     A = dequant_nvfp4_rows(a_codes, a_scales, a_sdec_rows)
     B = dequant_nvfp4(b_codes, b_scales, b_kind, b_sdec)
-    return A @ B.T
+    return _product(A, B, with_abs)
 
 
-def gemm_mxfp8(a_e4m3, a_e8m0, b_e4m3, b_e8m0):
+def gemm_mxfp8(a_e4m3, a_e8m0, b_e4m3, b_e8m0, with_abs=False):
     """D = A . B^T on exactly dequantized MXFP8 operands, float64."""
-    return dequant_mxfp8(a_e4m3, a_e8m0) @ dequant_mxfp8(b_e4m3, b_e8m0).T
+    return _product(dequant_mxfp8(a_e4m3, a_e8m0), dequant_mxfp8(b_e4m3, b_e8m0), with_abs)
 
 
 def round_bf16(x):

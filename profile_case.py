@@ -1,15 +1,19 @@
 """Run one library call on a given shape repeatedly: a small, self-contained case for
-profilers (e.g. ``ncu -k regex:gemm_kernel -s 2 -c 1 python -m
-mxfp8_precision_numerics_gb300.profile_case --call gemm_mxfp8 --M 8192 --N 4096 --K 16384``).
+profilers (e.g. ``ncu -k regex:gemm_pair_kernel -s 2 -c 1 python profile_case.py
+--call gemm_mxfp8 --M 8192 --N 4096 --K 16384``). The commands of the summaries under
+profiles/ run it.
 
 Operands are random bytes of the right formats generated on the device (values do not
 change the work any of these kernels does), so the case starts in seconds.
 """
 import argparse
+import os
+import sys
 
 import torch
 
-from . import fp4q as F
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+from mxfp8_precision_numerics_gb300 import fp4q as F  # noqa: E402
 
 
 def _e4m3(shape, g):

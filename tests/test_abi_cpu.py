@@ -48,6 +48,18 @@ def _lib(F):
     return F._lib
 
 
+def test_wait_timeout_test_hook_validates_before_any_launch(F):
+    L = _lib(F)
+    p = ctypes.c_void_p(256)
+    assert L.fp4q_test_gemm_wait_timeout(None, p, p, p, p, 512, 512, 1024, 20_000_000, None) == F.ERR_NULL
+    assert L.fp4q_test_gemm_wait_timeout(p, p, p, p, p, 512, 512, 1024, 10, None) == F.ERR_ARG
+    assert L.fp4q_test_gemm_wait_timeout(p, p, p, p, p, 512, 512, 1024, 3_000_000_000, None) == F.ERR_ARG
+    assert L.fp4q_test_gemm_wait_timeout(p, p, p, p, p, 128, 512, 1024, 20_000_000, None) == F.ERR_SHAPE
+    assert L.fp4q_test_gemm_wait_timeout(p, p, p, p, p, 512, 512, 640, 20_000_000, None) == F.ERR_SHAPE
+    assert L.fp4q_test_gemm_wait_timeout(ctypes.c_void_p(264), p, p, p, p, 512, 512, 1024, 20_000_000,
+                                         None) == F.ERR_ALIGN
+
+
 def test_validation_rejects_bad_arguments_without_touching_cuda(F):
     L = _lib(F)
     p = ctypes.c_void_p(16)            # an aligned dummy address: never dereferenced

@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import assert_bf16_near, assert_bf16_rounding_of, bf16_values, gelu64, gelu_grad64
+from helpers import assert_bf16_near, assert_bf16_rounding_of, bf16_values
 from mxfp8_precision_numerics_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -38,10 +38,9 @@ def test_nvfp4_gelu_epilogue(F, orc, M, N, K):
     # h is the plain GEMM's bf16 output, bit for bit, and within one ulp of the oracle
     assert np.array_equal(u16(h), u16(plain)), "h differs from the plain GEMM output"
     ref = orc.gemm_nvfp4(xc.cpu().numpy(), xs.cpu().numpy(), 1, float(xsd.item()),
-                         wc.cpu().numpy(), ws.cpu().numpy(), 2, float(wsd.item()))
+                         wc.cpu().numpy(), ws.cpu().numpy(), 2, float(wsd.item()), with_abs=True)
     assert_bf16_rounding_of(u16(h), ref, f"GELU GEMM h {M}x{N}x{K}")
-    hv = bf16_values(u16(h))
-    assert_bf16_near(u16(act), gelu64(hv), 1, f"GELU(h) {M}x{N}x{K}")
+    assert_bf16_near(u16(act), orc.gelu_bf16(u16(h)), 1, f"GELU(h) {M}x{N}x{K}")
     av = bf16_values(u16(act))
     assert float(amax.item()) == float(np.max(np.abs(av))), "amax is not max|GELU(h)|"
 
@@ -76,6 +75,6 @@ def test_mxfp8_dgelu_epilogue(F, orc, M, N, K):
     da = F.gemm_mxfp8(cu(a), cu(asc), cu(b), cu(bsc), torch.bfloat16)
     torch.cuda.synchronize()
     assert F.fp4q_device_status() == F.OK
-    assert_bf16_rounding_of(u16(da), orc.gemm_mxfp8(a, asc, b, bsc), f"dgrad {M}x{N}x{K}")
-    want = bf16_values(u16(da)).astype(np.float64) * gelu_grad64(bf16_values(I.bf16_bits(h)))
+    assert_bf16_rounding_of(u16(da), orc.gemm_mxfp8(a, asc, b, bsc, with_abs=True), f"dgrad {M}x{N}x{K}")
+    want = bf16_values(u16(da)).astype(np.float64) * orc.gelu_bf16(I.bf16_bits(h), grad=True)
     assert_bf16_near(u16(dh), want, 2, f"dGELU {M}x{N}x{K}")

@@ -82,7 +82,7 @@ def test_gemm_mxfp4_structured_scales(F, orc):
     d = F.gemm_mxfp4(cu(a), cu(ae), cu(b), cu(be))
     torch.cuda.synchronize()
     assert F.fp4q_device_status() == F.OK
-    assert_gemm_close(d.cpu().numpy(), orc.gemm_mxfp4(a, ae, b, be), "MXFP4 structured")
+    assert_gemm_close(d.cpu().numpy(), orc.gemm_mxfp4(a, ae, b, be, with_abs=True), "MXFP4 structured")
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 256, 2048), (300, 272, 4096), (128, 512, 2048), (1, 16, 2048)])
@@ -90,7 +90,7 @@ def test_gemm_mxfp4_random(F, orc, M, N, K):
     rng = np.random.default_rng(M + N + K)
     a, ae = rand_mxfp4(rng, M, K)
     b, be = rand_mxfp4(rng, N, K)
-    ref = orc.gemm_mxfp4(a, ae, b, be)
+    ref = orc.gemm_mxfp4(a, ae, b, be, with_abs=True)
     d = F.gemm_mxfp4(cu(a), cu(ae), cu(b), cu(be))
     db = F.gemm_mxfp4(cu(a), cu(ae), cu(b), cu(be), torch.bfloat16)
     torch.cuda.synchronize()
@@ -113,7 +113,7 @@ def test_mxfp4_linear_layer(F, orc):
         torch.cuda.synchronize()
         oxc, oxe = orc.quantize_mxfp4(I.bf16_bits(x), rht, SIGNS)
         owc, owe = orc.quantize_mxfp4(I.bf16_bits(w), rht, SIGNS)
-        assert_gemm_close(y.cpu().numpy(), orc.gemm_mxfp4(oxc, oxe, owc, owe), f"MXFP4 layer rht={rht}")
+        assert_gemm_close(y.cpu().numpy(), orc.gemm_mxfp4(oxc, oxe, owc, owe, with_abs=True), f"MXFP4 layer rht={rht}")
         ref = (x.float() @ w.float().t()).numpy()
         assert np.linalg.norm(y.cpu().numpy() - ref) / np.linalg.norm(ref) < 0.2
 
@@ -143,6 +143,6 @@ def test_mxfp4_format_comparison_full_size_sampled(F, orc):
         widx = torch.from_numpy(wrows).cuda()
         assert_bytes_equal(wc[widx].cpu().numpy(), oc, f"W codes rht={rht}")
         assert_bytes_equal(we[widx].cpu().numpy(), oe, f"W e8m0 rht={rht}")
-        ref = orc.gemm_mxfp4(xc[idx].cpu().numpy(), xe[idx].cpu().numpy(), wc.cpu().numpy(), we.cpu().numpy())
+        ref = orc.gemm_mxfp4(xc[idx].cpu().numpy(), xe[idx].cpu().numpy(), wc.cpu().numpy(), we.cpu().numpy(), with_abs=True)
         yb = y[idx].cpu().view(torch.int16).numpy().view(np.uint16)
         assert_bf16_rounding_of(yb, ref, f"MXFP4 16384x14336x4096 sampled rht={rht}")

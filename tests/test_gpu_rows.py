@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from helpers import (assert_bf16_near, assert_bf16_rounding_of, assert_bytes_equal, assert_gemm_close,
-                     bf16_values, gelu64)
+                     bf16_values)
 from mxfp8_precision_numerics_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -124,7 +124,7 @@ def test_gemm_nvfp4_rows(F, orc, M, N, K, two_d):
                           torch.tensor([bsd], dtype=torch.float32, device="cuda"))
     torch.cuda.synchronize()
     assert F.fp4q_device_status() == F.OK
-    assert_gemm_close(d.cpu().numpy(), orc.gemm_nvfp4_rows(a, asc, asd, b, bsc, kind, bsd),
+    assert_gemm_close(d.cpu().numpy(), orc.gemm_nvfp4_rows(a, asc, asd, b, bsc, kind, bsd, with_abs=True),
                       f"NVFP4 rows {M}x{N}x{K}")
 
 
@@ -148,7 +148,7 @@ def test_gemm_nvfp4_rows_grouped(F, orc, K):
         lo, hi = offs[g], offs[g + 1]
         if hi == lo:
             continue
-        ref = orc.gemm_nvfp4_rows(a[lo:hi], asc[lo:hi], asd[lo:hi], bs[g][0], bs[g][1], 2, float(bsd[g]))
+        ref = orc.gemm_nvfp4_rows(a[lo:hi], asc[lo:hi], asd[lo:hi], bs[g][0], bs[g][1], 2, float(bsd[g]), with_abs=True)
         assert_gemm_close(got[lo:hi], ref, f"group {g}")
 
 
@@ -166,9 +166,9 @@ def test_gemm_nvfp4_gelu_rows(F, orc, M, N, K):
     assert F.fp4q_device_status() == F.OK
     assert np.array_equal(u16(h), u16(plain))
     ref = orc.gemm_nvfp4_rows(xc.cpu().numpy(), xs.cpu().numpy(), xsd.cpu().numpy(),
-                              wc.cpu().numpy(), ws.cpu().numpy(), 2, float(wsd.item()))
+                              wc.cpu().numpy(), ws.cpu().numpy(), 2, float(wsd.item()), with_abs=True)
     assert_bf16_rounding_of(u16(h), ref, f"GELU rows GEMM h {M}x{N}x{K}")
-    assert_bf16_near(u16(act), gelu64(bf16_values(u16(h))), 1, f"GELU(h) rows {M}x{N}x{K}")
+    assert_bf16_near(u16(act), orc.gelu_bf16(u16(h)), 1, f"GELU(h) rows {M}x{N}x{K}")
 
 
 # ------------------------------------------------------------------ requantize from per-row input
@@ -224,7 +224,7 @@ def test_linear_layer_with_per_token_activations(F, orc):
     oc, os_, osd = orc.quantize_1d_rows(I.bf16_bits(x), True)
     assert_bytes_equal(saved.xq[0].cpu().numpy(), oc, "layer x codes")
     wc, ws, _, wsd = orc.quantize_2d(I.bf16_bits(w))
-    assert_gemm_close(y.cpu().numpy(), orc.gemm_nvfp4_rows(oc, os_, osd, wc, ws, 2, wsd), "layer y")
+    assert_gemm_close(y.cpu().numpy(), orc.gemm_nvfp4_rows(oc, os_, osd, wc, ws, 2, wsd, with_abs=True), "layer y")
     ref = (x.float() @ w.float().t()).numpy()
     assert np.linalg.norm(y.cpu().numpy() - ref) / np.linalg.norm(ref) < 0.15
     assert dx.shape == (M, K) and dw.shape == (N, K)

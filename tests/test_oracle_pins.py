@@ -907,3 +907,47 @@ def test_mxfp4_error_above_nvfp4_and_rht_on_heavy_tails(orc):
     assert sc == 2.0 ** orc.pow2_ceil_exponent(float(np.abs(v).max()), 6.0)
     want = [orc.e2m1_encode_rne(np.float32(vi / sc)) for vi in v]
     assert [int(c) for c in unpack_codes(codes)[0, :32]] == want
+
+
+# ---------------------------------------------------------------- GELU (4bit.vizuara.ai §13-14)
+def test_normal_cdf_and_erfc_against_printed_tables(orc):
+    """Phi and erfc at the points printed in standard tables (tests/golden/normal_cdf.txt),
+    including the far lower tail, where Phi computed as (1 + erf)/2 would cancel to zero."""
+    for kind, x, v in read_golden_rows("normal_cdf.txt"):
+        x, v = float(x), float(v)
+        got = orc.normal_cdf(x) if kind == "phi" else 2.0 * orc.normal_cdf(-x * math.sqrt(2.0))
+        assert abs(got - v) <= 1e-13 * abs(v), (kind, x, got, v)
+
+
+def test_gelu_closed_forms(orc):
+    """GELU(0) = 0 and GELU'(0) = Phi(0) = 1/2; GELU(x) - GELU(-x) = x (Phi(x) + Phi(-x) = 1);
+    GELU'(x) + GELU'(-x) = 1; GELU(x) -> x above and -> 0 below, with the tail value
+    x Phi(x) at -10 from the table."""
+    assert orc.gelu(0.0) == 0.0 and orc.gelu_grad(0.0) == 0.5
+    for x in np.linspace(-9.0, 9.0, 181):
+        x = float(x)
+        assert abs(orc.gelu(x) - orc.gelu(-x) - x) <= 1e-15 * max(1.0, abs(x))
+        assert abs(orc.gelu_grad(x) + orc.gelu_grad(-x) - 1.0) <= 1e-15
+    assert orc.gelu(10.0) == 10.0
+    assert abs(orc.gelu(-10.0) - (-10.0 * 7.61985302416052e-24)) <= 1e-13 * 7.62e-23
+    # the page's examples of the activation are bf16 tensors: the batch form agrees
+    h = inputs.bf16_bits(inputs.normal(4, 64, seed=5, std=3.0))
+    hv = (h.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.array_equal(orc.gelu_bf16(h), np.vectorize(orc.gelu)(hv))
+    assert np.array_equal(orc.gelu_bf16(h, grad=True), np.vectorize(orc.gelu_grad)(hv))
+
+
+def test_gelu_grad_is_the_derivative_of_gelu(orc):
+    """GELU' against a central difference of the oracle's own GELU (step 1e-5: truncation
+    error ~1e-11, rounding ~1e-11): a dropped term or a wrong sign in x phi(x) fails."""
+    d = 1e-5
+    for x in np.linspace(-8.0, 8.0, 321):
+        x = float(x)
+        fd = (orc.gelu(x + d) - orc.gelu(x - d)) / (2 * d)
+        assert abs(fd - orc.gelu_grad(x)) <= 1e-8, (x, fd, orc.gelu_grad(x))
+    # the density: phi(0) = 1/sqrt(2 pi), and phi integrates Phi (one Simpson panel check)
+    assert abs(orc.normal_pdf(0.0) - 0.3989422804014327) <= 1e-16
+    xs = np.linspace(-1.0, 1.0, 2001)
+    ys = np.array([orc.normal_pdf(float(v)) for v in xs])
+    simpson = (xs[1] - xs[0]) / 3 * (ys[0] + ys[-1] + 4 * ys[1:-1:2].sum() + 2 * ys[2:-1:2].sum())
+    assert abs(simpson - (orc.normal_cdf(1.0) - orc.normal_cdf(-1.0))) <= 1e-12
