@@ -80,6 +80,8 @@ struct Params {
     CUtensorMap tma_b;
     CUtensorMap tma_sfa;       // pair kernel: scale rows of A, box {16 B, 128 rows}
     CUtensorMap tma_sfb;       // pair kernel: scale rows of B, box {16 B, 256 rows (16 for 2D tiles)}
+    CUtensorMap tma_d;         // pair kernel, bf16 output by TMA store: d, box {32 columns, 32 rows}
+    CUtensorMap tma_d2;        // ... and d2 (GELU(h))
     const uint8_t* a_sc;
     const uint8_t* b_sc;
     int64_t sc_ld;             // scale bytes per row (K/16 NVFP4, K/32 MXFP8)
@@ -104,6 +106,8 @@ struct Params {
     const uint16_t* aux;
     float* amax_out;
     uint64_t wait_ns;          // pair kernel: the limit of every mbarrier wait
+    uint32_t sf_unit_bytes;    // pair kernel: bytes of one staged scale unit (A rows + B rows or tile rows)
+    int tma_epi;               // pair kernel: bf16 outputs leave through shared memory by TMA stores
     int no_copies;             // pair kernel, failure-detection test: the producers issue no copies
 };
 
@@ -526,6 +530,43 @@ __device__ __forceinline__ uint32_t leader_addr(const void* p) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(smem_u32(p)));
     return r;
 }
+// TMA store of a 2D box from this CTA's shared memory, and the bulk-group bookkeeping
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(map), "r"(smem_u32(src)), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// One row's 16 bf16 pairs (32 columns) into a 32-row x 64-byte staging box with the TMA's 64-byte
+// swizzle (16-byte chunk q of row r at chunk q ^ ((r >> 1) & 3)): a warp's 32 rows hit 8
+// distinct bank groups per store.
+__device__ __forceinline__ void stage_row32(uint8_t* box, int r, const uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(box + r * 64 + 16 * (q ^ ((r >> 1) & 3))) =
+            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+}
+// GELU of a quarter of a row chunk (8 bf16 values, pk[4 qq .. 4 qq + 3]) into o, and the running
+// max of |GELU| (bf16 magnitude bits): the arithmetic of epi_bf16's GELU path, value for value
+__device__ __forceinline__ void gelu_quarter(const uint32_t (&pk)[16], int qq, uint32_t (&o)[4], uint32_t& amax_bits) {
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t x = pk[4 * qq + i];
+        const float x0 = __uint_as_float(x << 16), x1 = __uint_as_float(x & 0xFFFF0000u);
+        float c0, c1, p0, p1;
+        norm_cdf_pdf2(x0, x1, c0, c1, p0, p1);
+        float o0, o1;
+        f32x2_unpack(f32x2_mul(f32x2_pack(x0, x1), f32x2_pack(c0, c1)), o0, o1);   // x Phi(x)
+        o[i] = pack_bf16x2(o0, o1);
+        m2 = __vmaxu2(m2, o[i] & 0x7FFF7FFFu);
+    }
+    amax_bits = max(amax_bits, max(m2 & 0xFFFFu, m2 >> 16));
+}
+
 // Arrive on a barrier of the pair (default semantics: the tensor-memory writes it publishes are
 // ordered by tcgen05.wait::st + tcgen05.fence::before_thread_sync; a cluster-scope release fence
 // here stalled every writer warp on every stage).
@@ -836,69 +877,103 @@ constexpr uint32_t kIdesc2Mxfp8 = (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3)
 constexpr uint32_t kIdesc2Mxfp4 = (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                                   (1u << 23) | ((uint32_t)(256 >> 4) << 24);
 
-// Scale writer step of the pair kernel: K-block `sub` of a staged unit (rows W bytes apart)
-// into tensor memory, in the layout the tensor core reads: scale row r at lane r mod 32,
-// column base + r/32. The tensor core's lane quarter q computes A rows 32q .. 32q+31 and reads
-// their scales from its own lanes only (column base + q), so warp q writes just that column of
-// the A scales; every quarter multiplies all 256 B rows, so each gets all B-scale columns.
+// Scale writer pass of the pair kernel: K-blocks sub0 and sub0 + 1 (sub0 even) of a staged unit
+// (rows W bytes apart) into tensor memory, in the layout the tensor core reads: scale row r at
+// lane r mod 32, column base + r/32. The tensor core's lane quarter q computes A rows 32q .. 32q+31
+// and reads their scales from its own lanes only (column base + q), so warp q writes just that
+// column of the A scales; every quarter multiplies all 256 B rows, so each gets all B-scale columns.
 // b2d: B holds one scale row per 16 rows (16 x 16 tiles).
+// The pass is split: load_pass_scales issues every shared-memory read of both K-blocks at once
+// (they queue behind the tensor core's operand reads, so their latency, not the tensor-memory
+// stores, set the writers' pace when each K-block's loads waited for the previous one's stores),
+// store_pass_scales writes the two slots once the caller has waited for them to be free.
+template <int kKind> struct PassScales;
+template <> struct PassScales<0> { uint4 a[2]; uint4 b[2][8]; };   // NVFP4: a 16-byte chunk per K-block
+template <> struct PassScales<1> { uint2 a; uint2 b[8]; };         // MXFP8: 4 bytes per K-block
+template <> struct PassScales<2> { uint4 a; uint4 b[8]; };         // MXFP4: both K-blocks in one chunk
+
 template <int kKind>
-__device__ __forceinline__ void write_unit_scales(const uint8_t* unit, int sub, bool b2d, uint32_t sf, int lane,
-                                                  int quarter) {
+__device__ __forceinline__ void load_pass_scales(const uint8_t* unit, int sub0, bool b2d, int lane, int quarter,
+                                                 PassScales<kKind>& v) {
     constexpr uint32_t W = sf_unit_w<kKind>();
     const uint8_t* a0 = unit;
     const uint8_t* b0 = unit + sf_unit_a<kKind>();
     static_assert(kKind == 1 || W == 64, "the FP4 swizzle below assumes 64-byte scale rows");
     const int ra = lane + 32 * quarter;
-    if (kKind == 2) {
-        // MXFP4 units (64-byte rows, same swizzle): K-block `sub` is the 8-byte half sub & 1 of
-        // chunk sub >> 1. Word 0 (scales 0-3) serves MMAs 0 and 1, word 1 (scales 4-7) MMAs 2 and 3
-        // (scale-factor ids 0 and 2 pick the byte pair). SFA: columns sf + quarter, sf + 4 +
-        // quarter; SFB: columns sf + 8 + c and sf + 16 + c (c = row / 32).
-        const int ch = sub >> 1;
-        const uint4 a = *reinterpret_cast<const uint4*>(a0 + ra * W + 16 * (ch ^ ((ra >> 1) & 3)));
-        uint32_t b0w[8], b1w[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const int r = lane + 32 * c;
-            const uint4 v = *reinterpret_cast<const uint4*>(b0 + r * W + 16 * (ch ^ ((r >> 1) & 3)));
-            b0w[c] = (sub & 1) ? v.z : v.x;
-            b1w[c] = (sub & 1) ? v.w : v.y;
-        }
-        tmem_st1(sf + 0 + quarter, (sub & 1) ? a.z : a.x);
-        tmem_st1(sf + 4 + quarter, (sub & 1) ? a.w : a.y);
-        tmem_st8(sf + 8, b0w);
-        tmem_st8(sf + 16, b1w);
-    } else if (kKind == 0) {
+    if constexpr (kKind == 0) {
         // NVFP4 units arrive with the TMA's 64-byte swizzle: the 16-byte chunk `sub` of row r
         // sits at chunk sub ^ ((r >> 1) & 3), so the 8 lanes of a quarter-warp read 8 distinct
         // bank groups
-        const uint4 a = *reinterpret_cast<const uint4*>(a0 + ra * W + 16 * (sub ^ ((ra >> 1) & 3)));
-        uint4 b[8];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            const int sub = sub0 + s;
+            v.a[s] = *reinterpret_cast<const uint4*>(a0 + ra * W + 16 * (sub ^ ((ra >> 1) & 3)));
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int r = b2d ? ((lane + 32 * c) >> 4) : lane + 32 * c;
+                v.b[s][c] = *reinterpret_cast<const uint4*>(b0 + r * W + 16 * (sub ^ ((r >> 1) & 3)));
+            }
+        }
+    } else if constexpr (kKind == 2) {
+        // MXFP4 units (64-byte rows, same swizzle): K-blocks sub0 and sub0 + 1 are the two 8-byte
+        // halves of chunk sub0 >> 1
+        const int ch = sub0 >> 1;
+        v.a = *reinterpret_cast<const uint4*>(a0 + ra * W + 16 * (ch ^ ((ra >> 1) & 3)));
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            const int r = b2d ? ((lane + 32 * c) >> 4) : lane + 32 * c;
-            b[c] = *reinterpret_cast<const uint4*>(b0 + r * W + 16 * (sub ^ ((r >> 1) & 3)));
+            const int r = lane + 32 * c;
+            v.b[c] = *reinterpret_cast<const uint4*>(b0 + r * W + 16 * (ch ^ ((r >> 1) & 3)));
         }
-        // MMA j: SFA in column sf + 4j + quarter; SFB in columns sf + 16 + 8j + c (c = row / 32),
-        // 32 consecutive columns: one x32 store
-        tmem_st1(sf + 0 + quarter, a.x);
-        tmem_st1(sf + 4 + quarter, a.y);
-        tmem_st1(sf + 8 + quarter, a.z);
-        tmem_st1(sf + 12 + quarter, a.w);
-        const uint32_t vb[32] = {b[0].x, b[1].x, b[2].x, b[3].x, b[4].x, b[5].x, b[6].x, b[7].x,
-                                 b[0].y, b[1].y, b[2].y, b[3].y, b[4].y, b[5].y, b[6].y, b[7].y,
-                                 b[0].z, b[1].z, b[2].z, b[3].z, b[4].z, b[5].z, b[6].z, b[7].z,
-                                 b[0].w, b[1].w, b[2].w, b[3].w, b[4].w, b[5].w, b[6].w, b[7].w};
-        tmem_st32(sf + 16, vb);
     } else {
-        const uint32_t a = *reinterpret_cast<const uint32_t*>(a0 + ra * W + 4 * sub);
-        uint32_t b[8];
+        // MXFP8: 4 bytes per K-block, the pair's 8 bytes adjacent
+        v.a = *reinterpret_cast<const uint2*>(a0 + ra * W + 4 * sub0);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) b[c] = *reinterpret_cast<const uint32_t*>(b0 + (lane + 32 * c) * W + 4 * sub);
-        // SFA in column sf + quarter, SFB in sf + 4 .. sf + 11 (byte j = MMA j)
-        tmem_st1(sf + quarter, a);
-        tmem_st8(sf + 4, b);
+        for (int c = 0; c < 8; ++c) v.b[c] = *reinterpret_cast<const uint2*>(b0 + (lane + 32 * c) * W + 4 * sub0);
+    }
+}
+
+template <int kKind>
+__device__ __forceinline__ void store_pass_scales(const PassScales<kKind>& v, uint32_t sf0, uint32_t sf1,
+                                                  int quarter) {
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        const uint32_t sf = s ? sf1 : sf0;
+        if constexpr (kKind == 0) {
+            // MMA j: SFA in column sf + 4j + quarter; SFB in columns sf + 16 + 8j + c (c = row / 32),
+            // 32 consecutive columns: one x32 store
+            const uint4 a = v.a[s];
+            const uint4(&b)[8] = v.b[s];
+            tmem_st1(sf + 0 + quarter, a.x);
+            tmem_st1(sf + 4 + quarter, a.y);
+            tmem_st1(sf + 8 + quarter, a.z);
+            tmem_st1(sf + 12 + quarter, a.w);
+            const uint32_t vb[32] = {b[0].x, b[1].x, b[2].x, b[3].x, b[4].x, b[5].x, b[6].x, b[7].x,
+                                     b[0].y, b[1].y, b[2].y, b[3].y, b[4].y, b[5].y, b[6].y, b[7].y,
+                                     b[0].z, b[1].z, b[2].z, b[3].z, b[4].z, b[5].z, b[6].z, b[7].z,
+                                     b[0].w, b[1].w, b[2].w, b[3].w, b[4].w, b[5].w, b[6].w, b[7].w};
+            tmem_st32(sf + 16, vb);
+        } else if constexpr (kKind == 2) {
+            // word 0 (scales 0-3) serves MMAs 0 and 1, word 1 (scales 4-7) MMAs 2 and 3 (scale-factor
+            // ids 0 and 2 pick the byte pair). SFA: columns sf + quarter, sf + 4 + quarter; SFB:
+            // columns sf + 8 + c and sf + 16 + c (c = row / 32)
+            uint32_t b0w[8], b1w[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                b0w[c] = s ? v.b[c].z : v.b[c].x;
+                b1w[c] = s ? v.b[c].w : v.b[c].y;
+            }
+            tmem_st1(sf + 0 + quarter, s ? v.a.z : v.a.x);
+            tmem_st1(sf + 4 + quarter, s ? v.a.w : v.a.y);
+            tmem_st8(sf + 8, b0w);
+            tmem_st8(sf + 16, b1w);
+        } else {
+            // SFA in column sf + quarter, SFB in sf + 4 .. sf + 11 (byte j = MMA j)
+            uint32_t b[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) b[c] = s ? v.b[c].y : v.b[c].x;
+            tmem_st1(sf + quarter, s ? v.a.y : v.a.x);
+            tmem_st8(sf + 4, b);
+        }
     }
 }
 
@@ -974,15 +1049,21 @@ __device__ __forceinline__ int pair_tile(const Params& p, int tile, uint32_t ran
 // accumulator to registers, releases it (tmem_empty) and stores while the next tile's MMAs run;
 // the producer and the writers run ahead into the next tile meanwhile.
 constexpr int kPairThreads = 448;   // 6 + 8 warps
+constexpr uint32_t kEpiStageBytes = 8 * 2 * 2048;   // TMA-store epilogue staging (1024-aligned)
+constexpr uint32_t kPairSmemMax = 227 * 1024;       // the opt-in limit of dynamic shared memory per CTA
+static_assert(Pair<0>::S * kPairStage + Pair<0>::R * (sf_unit_a<0>() + 16 * sf_unit_w<0>()) + kEpiStageBytes + 2048 <=
+              kPairSmemMax, "NVFP4 pair shared memory with the TMA-store epilogue");
 
 // The pair kernel's output path, fixed at compile time so that each instantiation carries one
 // epilogue (fewer live registers, no spills): 0 fp32, 1 bf16, 2 bf16 + GELU (epi 1),
 // 3 bf16 x GELU'(h) (epi 2), 4 the combine encode (epi 3); -1 reads d_bf16 and epi at run time
 // (one instantiation for the plain fp32 and bf16 outputs).
+// 5 and 6: bf16 + GELU and plain bf16 leaving through shared memory by TMA stores.
 template <int kOut>
 struct PairOut {
-    static constexpr bool kBf16 = kOut >= 1 && kOut <= 3;
-    static constexpr int kEpi = kOut < 0 ? -1 : kOut == 2 ? 1 : kOut == 3 ? 2 : kOut == 4 ? 3 : 0;
+    static constexpr bool kBf16 = (kOut >= 1 && kOut <= 3) || kOut >= 5;
+    static constexpr int kEpi = kOut < 0 ? -1 : (kOut == 2 || kOut == 5) ? 1 : kOut == 3 ? 2 : kOut == 4 ? 3 : 0;
+    static constexpr bool kTma = kOut >= 5;
 };
 __host__ __device__ constexpr int pair_out(int d_bf16, int epi) {
     return epi == 1 ? 2 : epi == 2 ? 3 : epi == 3 ? 4 : (d_bf16 ? 1 : 0);
@@ -993,14 +1074,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 gemm_pair_kernel(const __grid_constant__ Params p) {
     constexpr bool kBf16Out = PairOut<kOut>::kBf16;
     constexpr int kEpiMode = PairOut<kOut>::kEpi;
+    constexpr bool kTmaEpi = PairOut<kOut>::kTma;
     constexpr int S = Pair<kKind>::S, G = Pair<kKind>::G, R = Pair<kKind>::R, DU = Pair<kKind>::DU,
                   T = Pair<kKind>::T;
     constexpr uint32_t kSfCols = Cfg<kKind>::kSfColsPerStage;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sf_stage = smem + S * kPairStage;
-    constexpr uint32_t kSfUnit = sf_unit<kKind>(), kSfUnitA = sf_unit_a<kKind>(), kW = sf_unit_w<kKind>();
-    uint64_t* full = reinterpret_cast<uint64_t*>(sf_stage + R * kSfUnit);  // leader: pair TMA bytes
+    constexpr uint32_t kSfUnitA = sf_unit_a<kKind>(), kW = sf_unit_w<kKind>();
+    // a staged scale unit: A rows, then B rows (or, for 16 x 16 tile scales, 16 tile rows)
+    const uint32_t kSfUnit = p.sf_unit_bytes;
+    // bf16 outputs by TMA store: 8 epilogue warps x 2 staging boxes of 32 rows x 64 bytes
+    uint8_t* epi_stage = sf_stage + R * kSfUnit;
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi_stage + (kTmaEpi ? kEpiStageBytes : 0u));  // leader: pair TMA bytes
     uint64_t* empty = full + S;                                              // own: multicast commit
     uint64_t* sf_full = empty + S;                                           // own: scale TMA bytes
     uint64_t* sf_empty = sf_full + R;                                        // own: 4 writer warps
@@ -1176,13 +1262,14 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         for (int gk = 0; gk < total_kb; gk += 2) {
             const int u = gk / G, r = u % R, t0 = gk % T, t1 = (gk + 1) % T;
             if (!mbar_wait(&sf_full[r], (uint32_t)(u / R) & 1u, wl)) break;
+            // the staged unit's reads go out before the waits for the two tensor-memory slots
+            PassScales<kKind> v;
+            load_pass_scales<kKind>(sf_stage + r * kSfUnit, gk % G, p.b_sc_2d != 0, lane, warp, v);
             if (!mbar_wait_pair(T == S ? &empty[t0] : &sf_free[t0], ((uint32_t)(gk / T) & 1u) ^ 1u, wl)) break;
             if (!mbar_wait_pair(T == S ? &empty[t1] : &sf_free[t1], ((uint32_t)((gk + 1) / T) & 1u) ^ 1u, wl)) break;
             tc_fence_after();
-            write_unit_scales<kKind>(sf_stage + r * kSfUnit, gk % G, p.b_sc_2d != 0,
-                                     tmem + lane_base + kSfCol + (uint32_t)t0 * kSfCols, lane, warp);
-            write_unit_scales<kKind>(sf_stage + r * kSfUnit, (gk + 1) % G, p.b_sc_2d != 0,
-                                     tmem + lane_base + kSfCol + (uint32_t)t1 * kSfCols, lane, warp);
+            store_pass_scales<kKind>(v, tmem + lane_base + kSfCol + (uint32_t)t0 * kSfCols,
+                                     tmem + lane_base + kSfCol + (uint32_t)t1 * kSfCols, warp);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -1200,10 +1287,13 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         const uint32_t empty_leader = leader_addr(tmem_empty);
         const bool rows_sd = kKind == 0 && p.a_sdec_rows;
         uint32_t amax_bits = 0;
+        uint8_t* my_stage = epi_stage + 4096u * (uint32_t)(warp - 6);   // TMA-store epilogue boxes
+        uint32_t epi_chunk = 0;
         for (int ti = 0; ti < my_tiles; ++ti) {
             int64_t m0, n0;
             const int g = pair_tile(p, cid + ti * ncl, rank, m0, n0);
-            const int64_t row = m0 + 32 * q + lane;
+            const int64_t mrow0 = m0 + 32 * q;
+            const int64_t row = mrow0 + lane;
             const bool row_ok = row < p.goff[g + 1];
             const float b_sd = kKind == 0 ? p.b_s_dec[g] : 1.0f;
             const float alpha_t = kKind == 0 && !rows_sd ? __fmul_rn(p.a_s_dec[0], b_sd) : 1.0f;
@@ -1240,12 +1330,35 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_leader);
-                epi_bf16<0>(p, p0, row, row_ok, col0, amax_bits);
-                epi_bf16<0>(p, p1, row, row_ok, col0 + 32, amax_bits);
-                pack_chunk(ra, alpha, p0);
-                epi_bf16<0>(p, p0, row, row_ok, col0 + 64, amax_bits);
-                pack_chunk(rb, alpha, p1);
-                epi_bf16<0>(p, p1, row, row_ok, col0 + 96, amax_bits);
+                if (kTmaEpi) {
+                    // through the warp's two staging boxes (alternating), one TMA store per chunk
+                    auto tma_chunk = [&](const uint32_t (&pk)[16], int64_t col) {
+                        uint8_t* box = my_stage + 2048u * (epi_chunk & 1u);
+                        if (lane == 0) bulk_wait_read<1>();      // this box's store two chunks ago has read it
+                        __syncwarp();
+                        stage_row32(box, lane, pk);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (mrow0 < p.M && col < p.N) tma_store_2d(&p.tma_d, box, (int32_t)col, (int32_t)mrow0);
+                            bulk_commit();
+                        }
+                        ++epi_chunk;
+                    };
+                    tma_chunk(p0, col0);
+                    tma_chunk(p1, col0 + 32);
+                    pack_chunk(ra, alpha, p0);
+                    tma_chunk(p0, col0 + 64);
+                    pack_chunk(rb, alpha, p1);
+                    tma_chunk(p1, col0 + 96);
+                } else {
+                    epi_bf16<0>(p, p0, row, row_ok, col0, amax_bits);
+                    epi_bf16<0>(p, p1, row, row_ok, col0 + 32, amax_bits);
+                    pack_chunk(ra, alpha, p0);
+                    epi_bf16<0>(p, p0, row, row_ok, col0 + 64, amax_bits);
+                    pack_chunk(rb, alpha, p1);
+                    epi_bf16<0>(p, p1, row, row_ok, col0 + 96, amax_bits);
+                }
             } else if (kOut < 0 ? p.d_bf16 != 0 : kBf16Out) {
                 // bf16 output with GELU or GELU backward (or chosen at run time): each 32-column
                 // chunk is rounded to bf16 pairs as soon as it is in registers (64 registers for
@@ -1267,8 +1380,39 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(empty_leader);
+                if (kEpiMode == 1 && kTmaEpi) {
+                    // h and GELU(h) through the warp's two staging boxes, two TMA stores per chunk
+                    uint8_t* box_h = my_stage;
+                    uint8_t* box_a = my_stage + 2048u;
+                    // (not unrolled: the four packed chunks then sit in local memory instead of
+                    // spilling at the 128-register cap)
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        if (lane == 0) bulk_wait_read<0>();      // the previous chunk's stores have read both
+                        __syncwarp();
+                        stage_row32(box_h, lane, pk[c]);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) epi_bf16<kEpiMode>(p, pk[c], row, row_ok, col0 + 32 * c, amax_bits);
+                        for (int qq = 0; qq < 4; ++qq) {
+                            uint32_t o[4];
+                            gelu_quarter(pk[c], qq, o, amax_bits);
+                            *reinterpret_cast<uint4*>(box_a + lane * 64 + 16 * (qq ^ ((lane >> 1) & 3))) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int64_t col = col0 + 32 * c;
+                            if (mrow0 < p.M && col < p.N) {
+                                tma_store_2d(&p.tma_d, box_h, (int32_t)col, (int32_t)mrow0);
+                                tma_store_2d(&p.tma_d2, box_a, (int32_t)col, (int32_t)mrow0);
+                            }
+                            bulk_commit();
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) epi_bf16<kEpiMode>(p, pk[c], row, row_ok, col0 + 32 * c, amax_bits);
+                }
             } else {
                 // fp32 output: three chunks load together, the first is stored while the last
                 // loads into its registers, then tensor memory goes back to the MMAs (one chunk
@@ -1291,6 +1435,9 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
                 store_chunk<kEpiMode>(p, ra, row, row_ok, col0 + 96, alpha);
             }
         }
+        // every TMA store has read its staging box (and written its output) before the CTA ends
+        if (kTmaEpi && lane == 0) bulk_wait_all();
+        __syncwarp();
         epi_flush_amax(p, amax_bits, lane);
     }
 
@@ -1345,6 +1492,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t row
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2D bf16 tensor map over an output [rows][cols] for TMA stores: box {32 columns, 32 rows},
+// 64-byte swizzle (the epilogue's staging layout).
+bool make_map_bf16_out(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
 }
 
 template <int kKind>
@@ -1411,7 +1572,7 @@ cudaError_t launch_pair_out(const GemmArgs& a, cudaStream_t st) {
     cudaGetDevice(&dev);
     if (configured_device != dev) {
         cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<kKind, kOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)pair_smem_bytes<kKind>());
+                                             (int)kPairSmemMax);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
@@ -1452,6 +1613,16 @@ cudaError_t launch_pair_out(const GemmArgs& a, cudaStream_t st) {
     p.groups = a.groups;
     p.wait_ns = a.wait_limit_ns > 0 ? (uint64_t)a.wait_limit_ns : kTimeoutNs;
     p.no_copies = a.no_copies;
+    p.sf_unit_bytes = sf_unit_a<kKind>() + (b2d ? 16u : (uint32_t)kBN) * sf_unit_w<kKind>();
+    constexpr bool tma_epi = PairOut<kOut>::kTma;
+    if (tma_epi) {
+        if (!make_map_bf16_out(&p.tma_d, a.d, (uint64_t)a.N, (uint64_t)a.M)) return cudaErrorInvalidValue;
+        if (kOut == 5 && !make_map_bf16_out(&p.tma_d2, a.d2, (uint64_t)a.N, (uint64_t)a.M)) return cudaErrorInvalidValue;
+    }
+    p.tma_epi = tma_epi ? 1 : 0;
+    const uint32_t smem_bytes = Pair<kKind>::S * kPairStage + Pair<kKind>::R * p.sf_unit_bytes +
+                                (tma_epi ? kEpiStageBytes : 0u) + 1024 + 1024;
+    if (smem_bytes > kPairSmemMax) return cudaErrorInvalidValue;
     int64_t tiles_m = 0;
     for (int gi = 0; gi < a.groups; ++gi) {
         const int64_t lo = a.groups == 1 ? 0 : a.group_offsets[gi];
@@ -1481,7 +1652,7 @@ cudaError_t launch_pair_out(const GemmArgs& a, cudaStream_t st) {
         max_clusters = n;
     }
     const int64_t clusters = tiles < max_clusters ? tiles : max_clusters;
-    gemm_pair_kernel<kKind, kOut><<<(unsigned)(2 * clusters), kPairThreads, pair_smem_bytes<kKind>(), st>>>(p);
+    gemm_pair_kernel<kKind, kOut><<<(unsigned)(2 * clusters), kPairThreads, smem_bytes, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -1498,10 +1669,14 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t st) {
             if (out == 3) return launch_pair_out<1, 3>(a, st);
         }
     } else {
+        // NVFP4 bf16 outputs (plain or with GELU) of ungrouped GEMMs leave by TMA stores when the
+        // staging boxes fit beside 16 x 16 tile scales (the forward GEMMs' weights)
+        const bool tma = a.groups == 1 && a.b_scale_kind == 2 &&
+                         ((reinterpret_cast<uintptr_t>(a.d) | (out == 2 ? reinterpret_cast<uintptr_t>(a.d2) : 0)) & 15u) == 0;
         if (out == 0) return launch_pair_out<kKind, 0>(a, st);
-        if (out == 1) return launch_pair_out<kKind, 1>(a, st);
+        if (out == 1) return tma ? launch_pair_out<kKind, 6>(a, st) : launch_pair_out<kKind, 1>(a, st);
         if constexpr (kKind == 0) {
-            if (out == 2) return launch_pair_out<0, 2>(a, st);
+            if (out == 2) return tma ? launch_pair_out<0, 5>(a, st) : launch_pair_out<0, 2>(a, st);
             if (out == 4) return launch_pair_out<0, 4>(a, st);
         }
     }
