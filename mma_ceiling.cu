@@ -29,6 +29,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
                  : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
     return ok != 0;
 }
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{.reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// bounded spin on the non-blocking test
+__device__ __forceinline__ bool mbar_wait_test(uint64_t* bar, uint32_t parity, uint64_t limit) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_test(bar, parity)) return true;
+        if ((it & 255u) == 0 && globaltimer() - t0 > limit) { atomicOr(&g_err, 1u); return false; }
+    }
+}
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit) {
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 0;; ++it) {
@@ -78,12 +93,20 @@ __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t
 
 constexpr uint32_t kSmem = 200 * 1024;   // one CTA per SM
 
-template <int kKind, bool kPair>
+// kMode: 0 one commit at the end; 1 a commit after every K-block (4 MMAs); 2 two commits per
+// K-block; 3 / 4 a commit per K-block and, before issuing K-block g, a wait for the completion of
+// K-block g - 4 / g - 2 (the dependency a pipelined GEMM's stage reuse puts on the issuing thread);
+// 5 the same wait on K-block g - 8 (long complete); 6 the wait on g - 4 by the non-blocking test;
+// 7 two waits on long-complete K-blocks (g - 8, g - 7); 8 the wait on g - 4 between the K-block's
+// second and third MMA; 9 two waits (g - 4, g - 3) there; 10 one wait after the second MMA and one
+// after the third
+template <int kKind, bool kPair, int kMode = 0>
 __global__ void __launch_bounds__(128, 1) ceiling_kernel(int kblocks) {
     extern __shared__ uint8_t raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     uint64_t* done = reinterpret_cast<uint64_t*>(smem + 65536);
-    uint32_t* slot = reinterpret_cast<uint32_t*>(done + 1);
+    uint64_t* cb = done + 1;                       // per-K-block commit barriers (kMode > 0)
+    uint32_t* slot = reinterpret_cast<uint32_t*>(cb + 8);
     const int warp = threadIdx.x >> 5;
     const uint32_t rank = kPair ? cluster_rank() : 0;
     // operands: A 128 x 128 B at 0, B (pair: this CTA's 128 of 256 rows; single: 256 rows) at 16 KB
@@ -91,6 +114,7 @@ __global__ void __launch_bounds__(128, 1) ceiling_kernel(int kblocks) {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     if (threadIdx.x == 0) {
         mbar_init(done, 1);
+        for (int i = 0; i < 8; ++i) mbar_init(&cb[i], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -123,9 +147,36 @@ __global__ void __launch_bounds__(128, 1) ceiling_kernel(int kblocks) {
     if (rank == 0 && threadIdx.x == 0) {
         const uint32_t sa = smem_u32(smem), sb = sa + 16384;
         const uint32_t sf = tmem + 256;
+        constexpr int kDepth = kMode == 3 ? 4 : 2;
         for (int kb = 0; kb < kblocks; ++kb) {
+            if ((kMode == 3 || kMode == 4) && kb >= kDepth) {
+                const int g = kb - kDepth;
+                if (!mbar_wait(&cb[g % 8], (uint32_t)(g / 8) & 1u, 10000000000ull)) break;
+            }
+            if (kMode == 5 && kb >= 8) {
+                const int g = kb - 8;
+                if (!mbar_wait(&cb[g % 8], (uint32_t)(g / 8) & 1u, 10000000000ull)) break;
+            }
+            if (kMode == 6 && kb >= 4) {
+                const int g = kb - 4;
+                if (!mbar_wait_test(&cb[g % 8], (uint32_t)(g / 8) & 1u, 10000000000ull)) break;
+            }
+            if (kMode == 7 && kb >= 8) {
+                const int g = kb - 8;
+                if (!mbar_wait(&cb[g % 8], (uint32_t)(g / 8) & 1u, 10000000000ull)) break;
+                if (!mbar_wait(&cb[(g + 1) % 8], (uint32_t)((g + 1) / 8) & 1u, 10000000000ull)) break;
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+                if ((kMode == 8 || kMode == 9 || kMode == 10) && j == 2 && kb >= 4) {
+                    const int g = kb - 4;
+                    if (!mbar_wait(&cb[g % 8], (uint32_t)(g / 8) & 1u, 10000000000ull)) break;
+                    if (kMode == 9 && !mbar_wait(&cb[(g + 1) % 8], (uint32_t)((g + 1) / 8) & 1u, 10000000000ull)) break;
+                }
+                if (kMode == 10 && j == 3 && kb >= 4) {
+                    const int g = kb - 3;
+                    if (!mbar_wait(&cb[g % 8], (uint32_t)(g / 8) & 1u, 10000000000ull)) break;
+                }
                 if (kKind == 0)
                     mma<0, kPair>(tmem, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j), idesc, sf + 4 * j,
                                   sf + 16 + 8 * j, (kb | j) ? 1u : 0u);
@@ -136,6 +187,15 @@ __global__ void __launch_bounds__(128, 1) ceiling_kernel(int kblocks) {
                 } else
                     mma<1, kPair>(tmem, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
                                   idesc | ((uint32_t)j << 29) | ((uint32_t)j << 4), sf, sf + 4, (kb | j) ? 1u : 0u);
+            }
+            for (int c = 0; c < (kMode == 2 ? 2 : kMode > 0 ? 1 : 0); ++c) {   // one or two commits
+                uint64_t* bar = c ? &cb[(kb % 8) ^ 4] : &cb[kb % 8];
+                if (kPair)
+                    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                                 ::"r"(smem_u32(bar)), "h"((unsigned short)3) : "memory");
+                else
+                    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                                 ::"r"(smem_u32(bar)) : "memory");
             }
         }
         if (kPair)
@@ -155,9 +215,9 @@ __global__ void __launch_bounds__(128, 1) ceiling_kernel(int kblocks) {
     }
 }
 
-template <int kKind, bool kPair>
+template <int kKind, bool kPair, int kMode = 0>
 void run(const char* name, int sms, double seconds) {
-    auto kern = ceiling_kernel<kKind, kPair>;
+    auto kern = ceiling_kernel<kKind, kPair, kMode>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     int ctas = kPair ? (sms / 2) * 2 : sms;
     cudaLaunchConfig_t cfg = {};
@@ -239,5 +299,21 @@ int main() {
     run<2, false>("mxfp4 single 128x256x64", sms, 1.5);
     run<1, true>("mxfp8 pair 256x256x32 (again)", sms, 1.5);
     run<0, true>("nvfp4 pair 256x256x64 (again)", sms, 1.5);
+    run<1, true, 1>("mxfp8 pair, commit / K-block", sms, 1.0);
+    run<0, true, 1>("nvfp4 pair, commit / K-block", sms, 1.0);
+    run<1, true, 2>("mxfp8 pair, 2 commits / K-block", sms, 1.0);
+    run<0, true, 2>("nvfp4 pair, 2 commits / K-block", sms, 1.0);
+    run<1, true, 3>("mxfp8 pair, wait K-block g-4", sms, 1.0);
+    run<0, true, 3>("nvfp4 pair, wait K-block g-4", sms, 1.0);
+    run<1, true, 4>("mxfp8 pair, wait K-block g-2", sms, 1.0);
+    run<0, true, 4>("nvfp4 pair, wait K-block g-2", sms, 1.0);
+    run<0, true, 5>("nvfp4 pair, wait K-block g-8", sms, 1.0);
+    run<0, true, 6>("nvfp4 pair, test-wait K-block g-4", sms, 1.0);
+    run<0, true, 7>("nvfp4 pair, 2 waits g-8, g-7", sms, 1.0);
+    run<0, true, 8>("nvfp4 pair, wait g-4 after MMA 2", sms, 1.0);
+    run<0, true, 9>("nvfp4 pair, 2 waits after MMA 2", sms, 1.0);
+    run<0, true, 10>("nvfp4 pair, waits after MMA 2, 3", sms, 1.0);
+    run<1, true, 8>("mxfp8 pair, wait g-4 after MMA 2", sms, 1.0);
+    run<1, true, 10>("mxfp8 pair, waits after MMA 2, 3", sms, 1.0);
     return 0;
 }
