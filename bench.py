@@ -4,8 +4,9 @@ Workload (the configuration that passes through every step of the path): tokens 
 d_model 4096, ffn 16384; X ~ N(0,1) with 0.1% outliers x50, W1/W2 ~ N(0,0.02),
 dY ~ Student-t(3) * 1e-3, all bf16 and synthetic. One step = 1D quantize of X and of
 GELU(H), 16x16 quantize of W1 and W2, two NVFP4 GEMMs forward (GELU and max|GELU| in the
-first one's epilogue); four MXFP8 requants with stochastic rounding (two with the 16-point
-RHT) and two MXFP8 GEMMs per layer backward (GELU' in the second layer's dgrad epilogue).
+first one's epilogue); per layer backward, the four MXFP8 quantizations with stochastic rounding
+(two with the 16-point RHT; the output gradient's rowwise and transposed ones from one read of it)
+and two MXFP8 GEMMs (GELU' in the second layer's dgrad epilogue).
 The metric is the step's dense GEMM throughput (6 x 2 M D F FLOPs per step) in TFLOP/s.
 The line also reports the same step with the activations quantized per token row with
 Four Over Six block scales ("per_token_4over6"), timed separately, the MoE combine wire
@@ -49,6 +50,8 @@ BYTES_PER_ELEM = {
     "quantize_1d_given_amax": 2.0 + 0.5 + 1 / 16,
     "quantize_2d": 2.0 + 2.0 + 0.5 + 1 / 256,
     "requant_bf16": 2.0 + 1 + 1 / 32,
+    # the output gradient's rowwise and transposed quantizations from one read
+    "requant_bf16_dual": 2.0 + 2 * (1 + 1 / 32),
     "requant_nvfp4_1d": 0.5 + 1 / 16 + 1 + 1 / 32,
     "requant_nvfp4_2d": 0.5 + 1 / 256 + 1 + 1 / 32,
     # per-token form: one pass, no amax kernel (the 4-byte row scale is left out: < 0.1%)
@@ -203,11 +206,11 @@ def mlp_step(F, torch, ins, log, seed, signs, outer="tensor"):
 
 
 LAUNCHES_PER_STEP = {
-    "amax": 3, "quantize_1d": 2, "quantize_2d": 2, "gemm_nvfp4": 2, "requant": 8, "gemm_mxfp8": 4,
+    "amax": 3, "quantize_1d": 2, "quantize_2d": 2, "gemm_nvfp4": 2, "requant": 6, "gemm_mxfp8": 4,
 }
 # per-token form: the weights' two amax passes, no activation amax
 LAUNCHES_PER_STEP_ROWS = {
-    "amax": 2, "quantize_1d_rows": 2, "quantize_2d": 2, "gemm_nvfp4": 2, "requant": 8, "gemm_mxfp8": 4,
+    "amax": 2, "quantize_1d_rows": 2, "quantize_2d": 2, "gemm_nvfp4": 2, "requant": 6, "gemm_mxfp8": 4,
 }
 STEP_FLOPS = 6 * 2.0 * M_TOK * D_MODEL * F_FFN
 
@@ -425,12 +428,10 @@ def configs_section(F, torch, dev, peaks, peak_src, iters=10):
     fl3 = 2.0 * M * N * K
 
     def c3(L):
-        g = L("requant_bf16", M * N, F.requant_mxfp8, F.IN_BF16, dy, None, None, M, N, 0, 0, 0, F.SR, seed,
-              F.TAG_DY_ROWS)
+        g, gt = L("requant_bf16_dual", M * N, F.requant_bf16_dual, dy, 1, signs, F.SR, seed, F.TAG_DY_ROWS,
+                  F.TAG_DY_T)
         wt = L("requant_nvfp4_2d", N * K, F.requant_mxfp8, F.IN_NVFP4_2D, wc, ws, wsd, N, K, 1, 0, 0, F.SR, seed,
                F.TAG_WT)
-        gt = L("requant_bf16", M * N, F.requant_mxfp8, F.IN_BF16, dy, None, None, M, N, 1, 1, signs, F.SR, seed,
-               F.TAG_DY_T)
         xt = L("requant_nvfp4_1d", M * K, F.requant_mxfp8, F.IN_NVFP4_1D, xc, xs, xsd, M, K, 1, 1, signs, F.SR,
                seed, F.TAG_XT)
         L("gemm_mxfp8_dgrad", fl3, F.gemm_mxfp8, g[0], g[1], wt[0], wt[1], torch.bfloat16)
@@ -438,7 +439,8 @@ def configs_section(F, torch, dev, peaks, peak_src, iters=10):
 
     finish("backward_requant_8192x4096x4096", timed_calls(torch, dev, c3, iters),
            "dY 8192x4096 Student-t(3)*1e-3, X 8192x4096 N(0,1) (NVFP4 1D), W 4096x4096 N(0,0.02) (NVFP4 2D); "
-           "4 requants to MXFP8 with SR (RHT16 on the wgrad operands), dgrad bf16 + wgrad fp32",
+           "requants to MXFP8 with SR (dY rowwise + transposed with RHT16 from one read, X_q^T with RHT16, "
+           "W_q^T), dgrad bf16 + wgrad fp32",
            lambda k: round(2 * fl3 / (per_iter_ms(k) * 1e-3) / 1e12, 1),
            "TFLOP/s (dgrad + wgrad FLOPs / backward time incl. requants)")
     del dy, xc, xs, wc, ws

@@ -199,6 +199,24 @@ FP4Q_API int fp4q_requant_t_mxfp8_sr(int in_kind, const void* in, const uint8_t*
                             uint8_t* out_e4m3, uint8_t* out_e8m0, fp4q_stream_t stream);
 
 /*
+ * fp4q_requant_bf16_dual — the output gradient's two MXFP8 quantizations from one read of it:
+ * the rowwise one for dgrad and the transposed one (optionally with the 16-point transform) for
+ * wgrad ([VZ] §10: "the output gradient is quantized to MXFP8 twice, as it is and transposed";
+ * [NV] "Random Hadamard Transforms" for the wgrad operand). The results are exactly those of
+ *   fp4q_requant_t_mxfp8_sr(FP4Q_IN_BF16, in, ..., transpose = 0, rht = 0, ..., tag_rows, rows_*)
+ *   fp4q_requant_t_mxfp8_sr(FP4Q_IN_BF16, in, ..., transpose = 1, rht, ..., tag_t, t_*)
+ * with the same rounding and seed (each output keeps its own counter stream, tagged).
+ *   in bf16 [rows][cols]; rows_e4m3 [rows][cols], rows_e8m0 [rows][cols/32];
+ *   t_e4m3 [cols][rows], t_e8m0 [cols][rows/32].
+ *   rows, cols multiples of 32; in, rows_e4m3, t_e4m3 16-byte aligned; errors as
+ *   fp4q_requant_t_mxfp8_sr.
+ */
+FP4Q_API int fp4q_requant_bf16_dual(const void* in, int64_t rows, int64_t cols, int rht, uint32_t rht_signs,
+                    int rounding, uint64_t seed, uint32_t tag_rows, uint32_t tag_t,
+                    uint8_t* rows_e4m3, uint8_t* rows_e8m0, uint8_t* t_e4m3, uint8_t* t_e8m0,
+                    fp4q_stream_t stream);
+
+/*
  * fp4q_rht16 — the 16-point random Hadamard transform on its own, along rows.
  * [NV] "Random Hadamard Transforms"; [AC] "Hadamard rotations". Same arithmetic and order
  * as the transform inside fp4q_requant_t_mxfp8_sr.

@@ -159,6 +159,39 @@ int fp4q_requant_t_mxfp8_sr(int in_kind, const void* in, const uint8_t* in_scale
     return cuda_status(fp4q::launch_requant(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int fp4q_requant_bf16_dual(const void* in, int64_t rows, int64_t cols, int rht, uint32_t rht_signs,
+                           int rounding, uint64_t seed, uint32_t tag_rows, uint32_t tag_t,
+                           uint8_t* rows_e4m3, uint8_t* rows_e8m0, uint8_t* t_e4m3, uint8_t* t_e8m0,
+                           fp4q_stream_t stream) {
+    if (rht != 0 && rht != 1) return FP4Q_ERR_ARG;
+    if (rounding != FP4Q_RNE && rounding != FP4Q_SR) return FP4Q_ERR_ARG;
+    if (rht_signs > 0xFFFFu) return FP4Q_ERR_ARG;
+    if (!in || !rows_e4m3 || !rows_e8m0 || !t_e4m3 || !t_e8m0) return FP4Q_ERR_NULL;
+    if (rows < 32 || cols < 32 || rows % 32 != 0 || cols % 32 != 0) return FP4Q_ERR_SHAPE;
+    if (rows / 64 + 1 > 65535 || cols / 64 + 1 > 2147483647) return FP4Q_ERR_SHAPE;
+    if (!al16(in) || !al16(rows_e4m3) || !al16(t_e4m3)) return FP4Q_ERR_ALIGN;
+    if (int d = check_device()) return d;
+    fp4q::RequantArgs a;
+    a.in_kind = FP4Q_IN_BF16;
+    a.in = in;
+    a.in_scales = nullptr;
+    a.in_s_dec = nullptr;
+    a.rows = rows;
+    a.cols = cols;
+    a.transpose = 1;
+    a.rht = rht;
+    a.rht_signs = rht_signs;
+    a.rounding = rounding;
+    a.seed = seed;
+    a.tag = tag_t;
+    a.out_e4m3 = t_e4m3;
+    a.out_e8m0 = t_e8m0;
+    a.out2_e4m3 = rows_e4m3;
+    a.out2_e8m0 = rows_e8m0;
+    a.tag2 = tag_rows;
+    return cuda_status(fp4q::launch_requant(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fp4q_rht16(const void* in, int in_dtype, float* out, int64_t rows, int64_t cols,
                uint32_t signs, fp4q_stream_t stream) {
     if (in_dtype != FP4Q_F32 && in_dtype != FP4Q_BF16) return FP4Q_ERR_ARG;

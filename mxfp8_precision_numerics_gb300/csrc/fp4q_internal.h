@@ -37,6 +37,10 @@ struct RequantArgs {
     uint32_t tag;
     uint8_t* out_e4m3;
     uint8_t* out_e8m0;
+    // bf16 input only: a second, rowwise output from the same read (no transform, tag2)
+    uint8_t* out2_e4m3 = nullptr;
+    uint8_t* out2_e8m0 = nullptr;
+    uint32_t tag2 = 0;
 };
 cudaError_t launch_requant(const RequantArgs& a, cudaStream_t st);
 cudaError_t launch_combine_encode(const void* in, int in_bf16, int64_t rows, int64_t cols, uint32_t signs,

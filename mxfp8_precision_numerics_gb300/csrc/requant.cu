@@ -206,7 +206,9 @@ struct TStage {
     static constexpr uint32_t kBytes = kKind == 0 ? kTR * kTC * 2 : kTR * kTC / 2;   // 16 KB / 4 KB
 };
 
-template <int kKind, bool kRht, bool kSR>
+// kDual (bf16 input): the same staged tile also gives the rowwise output (out2, tag2, no
+// transform) — one read of the input for both of the output gradient's quantizations.
+template <int kKind, bool kRht, bool kSR, bool kDual = false>
 __global__ void __launch_bounds__(kTThreads) requant_t_kernel(RequantArgs a, int tiles_c, int n_tiles) {
     __shared__ __align__(16) uint8_t stage[2][TStage<kKind>::kBytes];
     __shared__ uint32_t sct[2][kKind == 0 ? 1 : kTR][8];   // per input row: f16x2 scales, signs folded
@@ -303,6 +305,40 @@ __global__ void __launch_bounds__(kTThreads) requant_t_kernel(RequantArgs a, int
                 mx_encode_half<kRht, kSR>(v, valid, a.seed, a.tag, (uint64_t)oidx, a.out_e4m3 + oidx,
                                           hb ? nullptr : a.out_e8m0 + (oidx >> 5));
             }
+            if (kDual) {
+                // rowwise: thread (row, blk) encodes input row `row`'s 32 values of block blk of
+                // this tile; its four 16-byte reads start at a row-dependent chunk, so that the
+                // warp's 8 rows x 4 blocks hit 8 distinct bank groups per read
+                const int row = tid >> 2, blk = tid & 3, g = (row >> 4) & 3;
+                const uint32_t* rw = reinterpret_cast<const uint32_t*>(&stage[buf][0]) + row * 64;
+                uint4 w[4];   // w[qq] = chunk (qq + row) & 3 of the block
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq)
+                    w[qq] = *reinterpret_cast<const uint4*>(rw + 4 * ((4 * blk + ((qq + row) & 3)) ^ (2 * g)));
+                // undo the rotation by row & 3 with two conditional rotations (selects, no
+                // dynamic register indexing): by 2, then by 1
+                const bool r2 = (row & 2) != 0, r1 = (row & 1) != 0;
+                uint4 u[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 a0 = w[i], a2 = w[(i + 2) & 3];
+                    u[i] = make_uint4(r2 ? a2.x : a0.x, r2 ? a2.y : a0.y, r2 ? a2.z : a0.z, r2 ? a2.w : a0.w);
+                }
+                float v[32];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 b0 = u[q], b1 = u[(q + 3) & 3];
+                    const uint4 c = make_uint4(r1 ? b1.x : b0.x, r1 ? b1.y : b0.y, r1 ? b1.z : b0.z, r1 ? b1.w : b0.w);
+                    bf16x2_to_f32(c.x, v + 8 * q);
+                    bf16x2_to_f32(c.y, v + 8 * q + 2);
+                    bf16x2_to_f32(c.z, v + 8 * q + 4);
+                    bf16x2_to_f32(c.w, v + 8 * q + 6);
+                }
+                const int64_t r = r0 + row, c = c0 + 32 * blk;
+                if (r < a.rows && c < a.cols)
+                    mx_encode_block<false, kSR>(v, a.seed, a.tag2, (uint64_t)(r * a.cols + c),
+                                                a.out2_e4m3 + r * a.cols + c, a.out2_e8m0 + (r * a.cols + c) / 32);
+            }
         } else {
             const uint8_t* src = &stage[buf][0] + (16 * grp) * 64 + (p ^ (16 * grp));
             const uint32_t* sc = &sct[buf][16 * grp][(p >> 3) ^ (2 * grp)];
@@ -375,6 +411,25 @@ __global__ void __launch_bounds__(256) rht16_kernel(const void* __restrict__ in,
 // ---------------------------------------------------------------------------------------
 template <int kKind, bool kRht, bool kSR>
 static void launch_requant_t(const RequantArgs& a, cudaStream_t st) {
+    if constexpr (kKind == 0) {
+        if (a.transpose && a.out2_e4m3) {   // bf16: transposed + rowwise from one read
+            const int64_t tiles_c = (a.cols + kTC - 1) / kTC, tiles_r = (a.rows + kTR - 1) / kTR;
+            const int64_t n_tiles = tiles_c * tiles_r;
+            static int per_sm[2][2] = {};
+            int& occ = per_sm[kRht ? 1 : 0][kSR ? 1 : 0];
+            if (occ <= 0) {
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, requant_t_kernel<0, kRht, kSR, true>,
+                                                                  kTThreads, 0) != cudaSuccess || occ < 1) {
+                    (void)cudaGetLastError();
+                    occ = 4;
+                }
+            }
+            int64_t g = (int64_t)num_sms() * occ;
+            if (g > n_tiles) g = n_tiles;
+            requant_t_kernel<0, kRht, kSR, true><<<(unsigned)g, kTThreads, 0, st>>>(a, (int)tiles_c, (int)n_tiles);
+            return;
+        }
+    }
     if (a.transpose) {
         const int64_t tiles_c = (a.cols + kTC - 1) / kTC, tiles_r = (a.rows + kTR - 1) / kTR;
         const int64_t n_tiles = tiles_c * tiles_r;

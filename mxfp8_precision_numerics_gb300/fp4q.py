@@ -51,6 +51,7 @@ _SIGS = {
     "fp4q_requant_t_mxfp8_sr": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _int, _u32, _int, _u64,
                                        _u32, _vp, _vp, _vp]),
     "fp4q_rht16": (_int, [_vp, _int, _vp, _i64, _i64, _u32, _vp]),
+    "fp4q_requant_bf16_dual": (_int, [_vp, _i64, _i64, _int, _u32, _int, _u64, _u32, _u32, _vp, _vp, _vp, _vp, _vp]),
     "fp4q_gemm_nvfp4": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _int, _i64, _i64, _i64, _int,
                                ctypes.POINTER(ctypes.c_int64), _vp]),
     "fp4q_gemm_nvfp4_rows": (_int, [_vp, _vp, _vp, _vp, _vp, _int, _vp, _vp, _int, _i64, _i64, _i64, _int,
@@ -141,6 +142,13 @@ def fp4q_requant_t_mxfp8_sr(in_kind, inp, in_scales, in_s_dec, rows, cols, trans
 def fp4q_rht16(inp, in_dtype, out, rows, cols, signs, stream=None):
     _check(_lib.fp4q_rht16(_ptr(inp), in_dtype, _ptr(out), rows, cols, int(signs), _stream(stream)),
            "fp4q_rht16")
+
+
+def fp4q_requant_bf16_dual(inp, rows, cols, rht, rht_signs, rounding, seed, tag_rows, tag_t, rows_e4m3, rows_e8m0,
+                           t_e4m3, t_e8m0, stream=None):
+    _check(_lib.fp4q_requant_bf16_dual(_ptr(inp), rows, cols, int(rht), int(rht_signs), rounding, int(seed),
+                                       int(tag_rows), int(tag_t), _ptr(rows_e4m3), _ptr(rows_e8m0), _ptr(t_e4m3),
+                                       _ptr(t_e8m0), _stream(stream)), "fp4q_requant_bf16_dual")
 
 
 def _offsets(group_row_offsets):
@@ -291,6 +299,20 @@ def requant_mxfp8(in_kind, inp, in_scales, in_s_dec, rows, cols, transpose, rht,
     fp4q_requant_t_mxfp8_sr(in_kind, inp, in_scales, in_s_dec, rows, cols, transpose, rht, rht_signs,
                             rounding, seed, tag, e4, e8, stream)
     return e4, e8
+
+
+def requant_bf16_dual(inp, rht, rht_signs, rounding, seed, tag_rows, tag_t, stream=None):
+    """bf16 [rows, cols] -> ((e4m3 [rows, cols], e8m0 [rows, cols/32]),
+    (e4m3 [cols, rows], e8m0 [cols, rows/32])): the rowwise and the transposed requantization
+    from one read."""
+    rows, cols = inp.shape
+    dev = inp.device
+    r4 = _empty((rows, cols), torch.uint8, dev)
+    r8 = _empty((rows, cols // 32), torch.uint8, dev)
+    t4 = _empty((cols, rows), torch.uint8, dev)
+    t8 = _empty((cols, rows // 32), torch.uint8, dev)
+    fp4q_requant_bf16_dual(inp, rows, cols, rht, rht_signs, rounding, seed, tag_rows, tag_t, r4, r8, t4, t8, stream)
+    return (r4, r8), (t4, t8)
 
 
 def rht16(inp, signs, stream=None):

@@ -72,15 +72,16 @@ def linear_backward(dy, saved, seed, rht_signs, dx_dtype=torch.bfloat16, stream=
     M, K, N = saved.M, saved.K, saved.N
     xc, xs, xsd = saved.xq
     wc, ws, wsd = saved.wq
+    # dy's two quantizations from one read: rowwise (blocks along N) for dgrad, transposed with
+    # the RHT (blocks and transform along tokens) for wgrad
+    g, gt = F.requant_bf16_dual(dy, 1, rht_signs, rounding, seed, F.TAG_DY_ROWS, F.TAG_DY_T, stream)
     # dgrad: dx[m, k] = sum_n dy[m, n] w[n, k]   (blocks along N on both operands)
-    g = F.requant_mxfp8(F.IN_BF16, dy, None, None, M, N, 0, 0, 0, rounding, seed, F.TAG_DY_ROWS, stream)
     wt = F.requant_mxfp8(F.IN_NVFP4_2D, wc, ws, wsd, N, K, 1, 0, 0, rounding, seed, F.TAG_WT, stream)
     if dgelu_h is not None:
         dx = F.gemm_mxfp8_dgelu(g[0], g[1], wt[0], wt[1], dgelu_h, stream)
     else:
         dx = F.gemm_mxfp8(g[0], g[1], wt[0], wt[1], dx_dtype, stream)
     # wgrad: dw[n, k] = sum_m dy[m, n] x[m, k]   (blocks and RHT along tokens)
-    gt = F.requant_mxfp8(F.IN_BF16, dy, None, None, M, N, 1, 1, rht_signs, rounding, seed, F.TAG_DY_T, stream)
     x_kind = F.IN_NVFP4_1D_ROWS if saved.x_rows else F.IN_NVFP4_1D
     xt = F.requant_mxfp8(x_kind, xc, xs, xsd, M, K, 1, 1, rht_signs, rounding, seed, F.TAG_XT, stream)
     dw = F.gemm_mxfp8(gt[0], gt[1], xt[0], xt[1], torch.float32, stream)
@@ -157,25 +158,22 @@ def mlp_step(x, w1, w2, dy, seed, rht_signs, outer="tensor", call=None):
     S["y"] = C("gemm_nvfp4", 2.0 * M * D * Fh, gemm2, ac, as_, ad, w2c, w2s, F.SCALE_2D, w2d, torch.bfloat16)
     # ---- backward, layer 2: dA = dY W2 (times GELU'(h) in the epilogue), dW2 = dY^T A_q
     sr = F.SR
-    S["g"] = C("requant_bf16", M * D, F.requant_mxfp8, F.IN_BF16, dy, None, None, M, D, 0, 0, 0, sr, seed,
-               F.TAG_DY_ROWS)
+    # dY's two quantizations (rowwise for dgrad; transposed with the RHT for wgrad) from one read
+    S["g"], S["gt"] = C("requant_bf16_dual", M * D, F.requant_bf16_dual, dy, 1, rht_signs, sr, seed,
+                        F.TAG_DY_ROWS, F.TAG_DY_T)
     S["w2t"] = C("requant_nvfp4_2d", D * Fh, F.requant_mxfp8, F.IN_NVFP4_2D, w2c, w2s, w2d, D, Fh, 1, 0, 0, sr,
                  seed, F.TAG_WT)
     S["dh"] = C("gemm_mxfp8", 2.0 * M * Fh * D, F.gemm_mxfp8_dgelu, *S["g"], *S["w2t"], S["h"])
-    S["gt"] = C("requant_bf16", M * D, F.requant_mxfp8, F.IN_BF16, dy, None, None, M, D, 1, 1, rht_signs, sr,
-                seed, F.TAG_DY_T)
     S["at"] = C("requant_nvfp4_1d", M * Fh, F.requant_mxfp8, x_kind, ac, as_, ad, M, Fh, 1, 1, rht_signs, sr,
                 seed, F.TAG_XT)
     S["dw2"] = C("gemm_mxfp8", 2.0 * D * Fh * M, F.gemm_mxfp8, *S["gt"], *S["at"], torch.float32)
     # ---- backward, layer 1: dX = dH W1, dW1 = dH^T X_q (its own counter stream)
     seed2 = seed ^ SEED2_OFFSET
-    S["g1"] = C("requant_bf16", M * Fh, F.requant_mxfp8, F.IN_BF16, S["dh"], None, None, M, Fh, 0, 0, 0, sr,
-                seed2, F.TAG_DY_ROWS)
+    S["g1"], S["g1t"] = C("requant_bf16_dual", M * Fh, F.requant_bf16_dual, S["dh"], 1, rht_signs, sr, seed2,
+                          F.TAG_DY_ROWS, F.TAG_DY_T)
     S["w1t"] = C("requant_nvfp4_2d", Fh * D, F.requant_mxfp8, F.IN_NVFP4_2D, w1c, w1s, w1d, Fh, D, 1, 0, 0, sr,
                  seed2, F.TAG_WT)
     S["dx"] = C("gemm_mxfp8", 2.0 * M * D * Fh, F.gemm_mxfp8, *S["g1"], *S["w1t"], torch.bfloat16)
-    S["g1t"] = C("requant_bf16", M * Fh, F.requant_mxfp8, F.IN_BF16, S["dh"], None, None, M, Fh, 1, 1,
-                 rht_signs, sr, seed2, F.TAG_DY_T)
     S["xt"] = C("requant_nvfp4_1d", M * D, F.requant_mxfp8, x_kind, xc, xs, xsd, M, D, 1, 1, rht_signs, sr,
                 seed2, F.TAG_XT)
     S["dw1"] = C("gemm_mxfp8", 2.0 * Fh * D * M, F.gemm_mxfp8, *S["g1t"], *S["xt"], torch.float32)
@@ -192,5 +190,6 @@ def mlp_kernel_launches(outer="tensor"):
     forward: amax + quantize_1d of x, quantize_1d of GELU(h) (its amax comes from the GELU
     GEMM's epilogue), 2 x (amax + quantize_2d of a weight), 2 NVFP4 GEMMs = 9 (outer="row":
     one per-row quantize for each activation, no activation amax: 8);
-    backward: 2 x (4 requant + 2 MXFP8 GEMMs) = 12."""
-    return 20 if outer == "row" else 21
+    backward: 2 x (3 requant, one of them the output gradient's two quantizations from one read,
+    + 2 MXFP8 GEMMs) = 10."""
+    return 18 if outer == "row" else 19

@@ -48,6 +48,16 @@ def _lib(F):
     return F._lib
 
 
+def test_requant_dual_validates_before_any_launch(F):
+    L = _lib(F)
+    p = ctypes.c_void_p(256)
+    assert L.fp4q_requant_bf16_dual(None, 64, 64, 1, 0, 1, 0, 2, 3, p, p, p, p, None) == F.ERR_NULL
+    assert L.fp4q_requant_bf16_dual(p, 64, 64, 2, 0, 1, 0, 2, 3, p, p, p, p, None) == F.ERR_ARG
+    assert L.fp4q_requant_bf16_dual(p, 64, 64, 1, 0x10000, 1, 0, 2, 3, p, p, p, p, None) == F.ERR_ARG
+    assert L.fp4q_requant_bf16_dual(p, 48, 64, 1, 0, 1, 0, 2, 3, p, p, p, p, None) == F.ERR_SHAPE
+    assert L.fp4q_requant_bf16_dual(ctypes.c_void_p(264), 64, 64, 1, 0, 1, 0, 2, 3, p, p, p, p, None) == F.ERR_ALIGN
+
+
 def test_wait_timeout_test_hook_validates_before_any_launch(F):
     L = _lib(F)
     p = ctypes.c_void_p(256)

@@ -133,3 +133,31 @@ def test_rht16_matches_oracle(F, orc, bf16):
     want = orc.rht16(xo, 0xBEEF, is_bf16=bf16)
     got = out.cpu().numpy()
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("rows,cols,rht", [(64, 128, 1), (96, 160, 1), (256, 544, 0), (8192, 4096, 1)])
+def test_requant_bf16_dual_equals_the_two_calls(F, orc, rows, cols, rht):
+    """fp4q_requant_bf16_dual: the rowwise and the transposed (RHT) quantizations of the output
+    gradient from one read are the two separate requantizations, byte for byte (ragged 64 x 128
+    tiles included), and sampled rows match the oracle."""
+    seed, signs = I.sr_seed(7), I.rht_signs(7)
+    dy = I.student_t(rows, cols, seed=rows + cols)
+    d = dy.cuda()
+    (r4, r8), (t4, t8) = F.requant_bf16_dual(d, rht, signs, F.SR, seed, F.TAG_DY_ROWS, F.TAG_DY_T)
+    g4, g8 = F.requant_mxfp8(F.IN_BF16, d, None, None, rows, cols, 0, 0, 0, F.SR, seed, F.TAG_DY_ROWS)
+    u4, u8 = F.requant_mxfp8(F.IN_BF16, d, None, None, rows, cols, 1, rht, signs, F.SR, seed, F.TAG_DY_T)
+    torch.cuda.synchronize()
+    assert F.fp4q_device_status() == F.OK
+    for got, want, what in ((r4, g4, "rows e4m3"), (r8, g8, "rows e8m0"), (t4, u4, "T e4m3"), (t8, u8, "T e8m0")):
+        assert_bytes_equal(got.cpu().numpy(), want.cpu().numpy(), what)
+    db = I.bf16_bits(dy)
+    for b in (0, rows - 2):
+        o4, o8 = orc.requant_mxfp8(0, db, None, 1.0, rows, cols, False, False, 0, orc.SR, seed, F.TAG_DY_ROWS,
+                                   out_rows=(b, b + 2))
+        assert_bytes_equal(r4[b:b + 2].cpu().numpy(), o4, "rows e4m3 vs oracle")
+        assert_bytes_equal(r8[b:b + 2].cpu().numpy(), o8, "rows e8m0 vs oracle")
+    for b in (0, cols - 2):
+        o4, o8 = orc.requant_mxfp8(0, db, None, 1.0, rows, cols, True, bool(rht), signs, orc.SR, seed, F.TAG_DY_T,
+                                   out_rows=(b, b + 2))
+        assert_bytes_equal(t4[b:b + 2].cpu().numpy(), o4, "T e4m3 vs oracle")
+        assert_bytes_equal(t8[b:b + 2].cpu().numpy(), o8, "T e8m0 vs oracle")
