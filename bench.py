@@ -399,7 +399,43 @@ def configs_section(F, torch, dev, peaks, peak_src, iters=10):
     finish("linear_fwd_256x512", timed_calls(torch, dev, c1, iters),
            "X 256x512 N(0,1)+0.1% x50, W 256x512 N(0,0.02); 1D + 2D quantize, NVFP4 GEMM fp32 out",
            lambda k: round(per_iter_ms(k) * 1e3, 2), "us per forward (launch-latency bound)")
-    del x, w
+    # the same forward (5 kernels) captured once in a CUDA graph and replayed: the host's per-call
+    # overhead leaves the measurement; L2 flushed before every replay
+    def c1_direct():
+        xc, xs, xsd, _ = F.quantize_1d(x)
+        wc, ws, wsd, _ = F.quantize_2d(w)
+        return F.gemm_nvfp4(xc, xs, xsd, wc, ws, F.SCALE_2D, wsd, torch.float32)
+
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            c1_direct()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        c1_direct()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    times = []
+    for i in range(3 + iters):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(e0.elapsed_time(e1))
+    st = F.fp4q_device_status()
+    if st != F.OK:
+        raise RuntimeError("device status after the graph replays: " + F.status_str(st))
+    out["linear_fwd_256x512"]["graph"] = {
+        "what": "the forward's five kernels (amax + quantize of X, amax + quantize of W, GEMM) as one CUDA graph, "
+                "replayed; L2 flushed before each replay",
+        "value": round(statistics.mean(times) * 1e3, 2), "best": round(min(times) * 1e3, 2),
+        "unit": "us per forward", "replays": iters}
+    del graph, flush, x, w
 
     # ---- MoE expert forward: 8 experts x 1024 tokens, K 4096, N 1536 (up projection)
     E, T, K, N = 8, 8192, 4096, 1536

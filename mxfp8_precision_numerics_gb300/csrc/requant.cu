@@ -307,17 +307,18 @@ __global__ void __launch_bounds__(kTThreads) requant_t_kernel(RequantArgs a, int
             }
             if (kDual) {
                 // rowwise: thread (row, blk) encodes input row `row`'s 32 values of block blk of
-                // this tile; its four 16-byte reads start at a row-dependent chunk, so that the
-                // warp's 8 rows x 4 blocks hit 8 distinct bank groups per read
+                // this tile; its four 16-byte reads start at chunk rot = 2 (row & 1) + blk / 2, so
+                // that each quarter-warp (two rows x four blocks) reads 8 distinct bank groups
                 const int row = tid >> 2, blk = tid & 3, g = (row >> 4) & 3;
+                const int rot = 2 * (row & 1) + (blk >> 1);
                 const uint32_t* rw = reinterpret_cast<const uint32_t*>(&stage[buf][0]) + row * 64;
-                uint4 w[4];   // w[qq] = chunk (qq + row) & 3 of the block
+                uint4 w[4];   // w[qq] = chunk (qq + rot) & 3 of the block
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq)
-                    w[qq] = *reinterpret_cast<const uint4*>(rw + 4 * ((4 * blk + ((qq + row) & 3)) ^ (2 * g)));
-                // undo the rotation by row & 3 with two conditional rotations (selects, no
-                // dynamic register indexing): by 2, then by 1
-                const bool r2 = (row & 2) != 0, r1 = (row & 1) != 0;
+                    w[qq] = *reinterpret_cast<const uint4*>(rw + 4 * ((4 * blk + ((qq + rot) & 3)) ^ (2 * g)));
+                // undo the rotation with two conditional rotations (selects, no dynamic register
+                // indexing): by 2, then by 1
+                const bool r2 = (rot & 2) != 0, r1 = (rot & 1) != 0;
                 uint4 u[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {

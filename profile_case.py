@@ -25,7 +25,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--call", required=True,
                     choices=["gemm_mxfp8", "gemm_mxfp8_dgelu", "gemm_nvfp4", "gemm_nvfp4_gelu", "gemm_mxfp4", "quantize_1d",
-                             "quantize_2d",
+                             "quantize_1d_given_amax", "quantize_2d", "requant_bf16_dual", "mlp_step",
                              "quantize_1d_rows46", "quantize_mxfp4", "requant_bf16_t_rht", "requant_bf16_rows",
                              "requant_nvfp4_t_rht", "requant_nvfp4_2d_t", "combine_encode", "combine_decode"])
     ap.add_argument("--M", type=int, default=8192)
@@ -35,6 +35,7 @@ def main():
     ap.add_argument("--k", type=int, default=1, help="combine_decode: arrivals per token (M tokens)")
     ap.add_argument("--bf16", action="store_true", help="combine: bf16 encode input / decode output")
     ap.add_argument("--rht", action="store_true", help="quantize_mxfp4: rotate by RHT32 first")
+    ap.add_argument("--f32", action="store_true", help="gemm_mxfp8: fp32 output (default bf16)")
     a = ap.parse_args()
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
@@ -43,7 +44,7 @@ def main():
         A, B = _e4m3((M, K), g), _e4m3((N, K), g)
         As = torch.randint(120, 134, (M, K // 32), dtype=torch.uint8, device="cuda", generator=g)
         Bs = torch.randint(120, 134, (N, K // 32), dtype=torch.uint8, device="cuda", generator=g)
-        fn = lambda: F.gemm_mxfp8(A, As, B, Bs, torch.bfloat16)
+        fn = lambda: F.gemm_mxfp8(A, As, B, Bs, torch.float32 if a.f32 else torch.bfloat16)
     elif a.call == "gemm_mxfp8_dgelu":
         A, B = _e4m3((M, K), g), _e4m3((N, K), g)
         As = torch.randint(120, 134, (M, K // 32), dtype=torch.uint8, device="cuda", generator=g)
@@ -66,6 +67,14 @@ def main():
         As = torch.randint(118, 136, (M, K // 32), dtype=torch.uint8, device="cuda", generator=g)
         Bs = torch.randint(118, 136, (N, K // 32), dtype=torch.uint8, device="cuda", generator=g)
         fn = lambda: F.gemm_mxfp4(A, As, B, Bs, torch.bfloat16)
+    elif a.call == "mlp_step":
+        # the benchmark's step (tokens M, d_model N, ffn K): synthetic normal inputs on the device
+        from mxfp8_precision_numerics_gb300 import layer
+        x = torch.randn(M, N, device="cuda", generator=g).to(torch.bfloat16)
+        w1 = (torch.randn(K, N, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        w2 = (torch.randn(N, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        dy = (torch.randn(M, N, device="cuda", generator=g) * 1e-3).to(torch.bfloat16)
+        fn = lambda: layer.mlp_step(x, w1, w2, dy, 12345, 0xA5C3)
     elif a.call == "combine_encode":
         y = torch.randn(M, K, device="cuda", generator=g)
         if a.bf16:
@@ -78,6 +87,11 @@ def main():
         x = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
         if a.call == "quantize_1d":
             fn = lambda: F.quantize_1d(x)
+        elif a.call == "quantize_1d_given_amax":
+            amax = x.float().abs().max().reshape(1)
+            fn = lambda: F.quantize_1d(x, amax_in=amax)
+        elif a.call == "requant_bf16_dual":
+            fn = lambda: F.requant_bf16_dual(x, 1, 0xA5C3, F.SR, 1, 2, 3)
         elif a.call == "quantize_1d_rows46":
             fn = lambda: F.quantize_1d_rows(x, True)
         elif a.call == "quantize_mxfp4":
