@@ -215,9 +215,12 @@ LAUNCHES_PER_STEP_ROWS = {
 STEP_FLOPS = 6 * 2.0 * M_TOK * D_MODEL * F_FFN
 
 
-def summarize_kernels(kinds, peaks, peak_src="measured", region_s=0.0):
+def summarize_kernels(kinds, peaks, peak_src="measured", region_s=0.0, traffic_kinds=None):
     """Per call kind: launches, average duration and achieved rate against its roofline
-    (GEMMs against the tensor peak gemm_peak picks for a timed region of region_s seconds)."""
+    (GEMMs against the tensor peak gemm_peak picks for a timed region of region_s seconds).
+    DRAM traffic comes from the committed ncu captures, which were taken at the MLP step's
+    shapes (and the weight sweep's largest GEMM): traffic_kinds lists the kinds that run at
+    those shapes here (None: all, the step itself); the others report null."""
     kernels = {}
     for kind, (n, tot_ms, units) in sorted(kinds.items()):
         avg = tot_ms / n
@@ -239,7 +242,8 @@ def summarize_kernels(kinds, peaks, peak_src="measured", region_s=0.0):
                              "peak": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4),
                              "peak_source": f"{peak_src} HBM copy",
                              "algorithmic_per_launch": f"{units / n * bpe:.4g} B"}
-        kernels[kind]["traffic"] = ncu_traffic(kind)      # DRAM bytes per launch (ncu), or None
+        # DRAM bytes per launch (ncu), or None
+        kernels[kind]["traffic"] = ncu_traffic(kind) if traffic_kinds is None or kind in traffic_kinds else None
     return kernels
 
 
@@ -285,7 +289,7 @@ def combine_section(F, torch, dev, peaks, iters=10):
         raise RuntimeError("device status after the combine section: " + F.status_str(st))
     return {"workload": f"MoE combine: {T} tokens x d_model {D}, {E} experts x {T // E} tokens (top-1), "
                         f"expert ffn {FE}; decode k=2 on {2 * T} arrivals; inputs N(0,1) / Student-t(3)",
-            "iterations": iters, "kernels": summarize_kernels(log.totals(), peaks, "measured")}
+            "iterations": iters, "kernels": summarize_kernels(log.totals(), peaks, "measured", traffic_kinds=())}
 
 
 def format_section(F, torch, dev, peaks, iters=10):
@@ -323,7 +327,8 @@ def format_section(F, torch, dev, peaks, iters=10):
     if st != F.OK:
         raise RuntimeError("device status after the format section: " + F.status_str(st))
     return {"workload": f"X {M}x{K} N(0,1)+0.1% x50, W {N}x{K} N(0,0.02); bf16 GEMM outputs",
-            "iterations": iters, "kernels": summarize_kernels(log.totals(), peaks, "measured")}
+            "iterations": iters,
+            "kernels": summarize_kernels(log.totals(), peaks, "measured", traffic_kinds=("quantize_1d",))}
 
 
 FLUSH_BYTES = 256 << 20      # written between timed iterations: twice the 129 MB L2
@@ -373,10 +378,10 @@ def configs_section(F, torch, dev, peaks, peak_src, iters=10):
     from mxfp8_precision_numerics_gb300 import inputs as I
     out = {}
 
-    def finish(name, log, workload, value, unit, extra=None):
+    def finish(name, log, workload, value, unit, extra=None, traffic_kinds=()):
         kinds = log.totals()
         region_s = sum(t for _, t, _ in kinds.values()) * 1e-3
-        kern = summarize_kernels(kinds, peaks, peak_src, region_s)
+        kern = summarize_kernels(kinds, peaks, peak_src, region_s, traffic_kinds)
         dom = max(kinds.items(), key=lambda kv: kv[1][1])[0]
         rec = {"workload": workload, "iterations": iters, "value": value(kinds), "unit": unit,
                "kernels": kern, "roofline": roofline_of(kern, dom)}
@@ -498,7 +503,7 @@ def configs_section(F, torch, dev, peaks, peak_src, iters=10):
            "W 14336x4096 N(0,0.02) (2D quantize), X Mx4096 N(0,1) for M in 1024/4096/16384 (1D quantize), "
            "NVFP4 GEMM bf16 out",
            lambda k: round(2.0 * 16384 * N * K / (k["gemm_nvfp4_M16384"][1] / iters * 1e-3) / 1e12, 1),
-           "TFLOP/s (NVFP4 GEMM at M=16384)")
+           "TFLOP/s (NVFP4 GEMM at M=16384)", traffic_kinds=("gemm_nvfp4_M16384",))
     return out
 
 
@@ -687,7 +692,9 @@ def run_ours(args, rank, world, local_rank):
             "value": round(STEP_FLOPS / (r_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(r_ms, 4), "steps": r_steps, "warmup": 3,
             "gpu_launches": int(sum(LAUNCHES_PER_STEP_ROWS.values()) * r_steps),
-            "kernels": summarize_kernels(rlog.totals(), peaks, peak_src, r_ms * r_steps * 1e-3),
+            # traffic: only the kernels this form shares with the per-tensor step
+            "kernels": summarize_kernels(rlog.totals(), peaks, peak_src, r_ms * r_steps * 1e-3,
+                                         ("gemm_mxfp8", "quantize_2d", "requant_nvfp4_2d")),
         },
     }
     with ClockSampler(smi_id) as clk2:
