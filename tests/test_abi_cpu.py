@@ -190,3 +190,32 @@ def test_product_path_has_no_oracle_or_fallback():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "liboracle" not in text, f
+
+
+def test_empty_inputs_are_rejected_before_any_launch(F):
+    """A zero (or negative) size in any dimension is FP4Q_ERR_SHAPE at every entry point, checked
+    on the host: no kernel is launched for an empty tensor (the header states the minimum sizes)."""
+    L = _lib(F)
+    p = ctypes.c_void_p(256)
+    n = None
+    S = F.ERR_SHAPE
+    for rows, cols in ((0, 32), (16, 0), (-16, 32)):
+        assert L.fp4q_quantize_1d(p, rows, cols, 32, n, p, p, p, p, n) == S
+        assert L.fp4q_quantize_1d_rows(p, rows, cols, 32, 1, p, p, p, n) == S
+        assert L.fp4q_quantize_2d(p, rows, cols, 32, 1, 0, n, p, p, p, p, n) == S
+        assert L.fp4q_quantize_2d_noalloc(p, rows, cols, 32, 1, 0, p, p, p, n) == S
+        assert L.fp4q_quantize_mxfp4(p, rows, cols, 32, 0, 0, p, p, n) == S
+        assert L.fp4q_rht16(p, 0, p, rows, cols, 0, n) == S
+        assert L.fp4q_combine_encode(p, 0, rows, cols, 0, p, p, n) == S
+    for rows, cols in ((0, 64), (64, 0)):
+        for kind in (0, 1, 2):
+            assert L.fp4q_requant_t_mxfp8_sr(kind, p, p, p, rows, cols, 1, 0, 0, 1, 0, 0, p, p, n) == S
+        assert L.fp4q_requant_bf16_dual(p, rows, cols, 1, 0, 1, 0, 2, 3, p, p, p, p, n) == S
+    assert L.fp4q_combine_decode(p, p, 0, 2, 64, 0, p, 0, n) == S
+    for M, N, K in ((0, 256, 256), (128, 0, 256), (128, 256, 0)):
+        assert L.fp4q_gemm_nvfp4(p, p, p, p, p, 1, p, p, 0, M, N, K, 1, None, n) == S
+        assert L.fp4q_gemm_nvfp4_rows(p, p, p, p, p, 1, p, p, 0, M, N, K, 1, None, n) == S
+        assert L.fp4q_gemm_nvfp4_gelu(p, p, p, p, p, 2, p, p, p, p, M, N, K, n) == S
+        assert L.fp4q_gemm_mxfp8(p, p, p, p, p, 0, M, N, K, n) == S
+        assert L.fp4q_gemm_mxfp8_dgelu(p, p, p, p, p, p, M, N, K, n) == S
+        assert L.fp4q_gemm_mxfp4(p, p, p, p, p, 0, M, N, max(K, 0) * 8, n) == S
