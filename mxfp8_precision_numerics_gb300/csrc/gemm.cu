@@ -842,21 +842,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 //   R   scale units staged in shared memory
 //   DU  how many units the scale loads run ahead of the A/B loads
 //   T   scale slots in tensor memory (written by warps 0-3, read by the MMAs)
+//   KPS K-blocks per barrier group (1 or 2)
 // Scales travel by TMA (async proxy, no load/store-unit traffic: per-row 4-byte copies
 // through L1 took most of the shared-memory bandwidth the tensor core needs) in boxes W bytes
 // wide: the TMA unit's cost grows with the rows of a box, so narrow scale boxes issued every
 // K-block held back the A/B loads. Their loads run DU units ahead of the A/B loads, and the
 // writers may fill up to T tensor-memory slots ahead of the MMAs.
+// KPS K-blocks share one pair of full/empty barriers (one expect_tx, one wait, one commit per
+// group) and one scale-slot handshake (the writers' pass stores both slots of a pair anyway):
+// for MXFP8, whose K-block is half as deep as the 4-bit kinds', it halves the barrier round
+// trips per FLOP.
 // Tensor memory: 256 accumulator columns + T x kSfColsPerStage <= 512.
 template <int kKind> struct Pair;
-template <> struct Pair<0> { static constexpr int S = 5, G = 4, R = 2, DU = 1, T = 5; };
-template <> struct Pair<1> { static constexpr int S = 6, G = 4, R = 3, DU = 2, T = 16; };
+template <> struct Pair<0> { static constexpr int S = 5, G = 4, R = 2, DU = 1, T = 5, KPS = 1; };
+template <> struct Pair<1> { static constexpr int S = 6, G = 4, R = 3, DU = 2, T = 16, KPS = 2; };
 // MXFP4: units of 8 K-blocks, so that a unit's scale rows are 64 bytes like NVFP4's (same swizzle)
-template <> struct Pair<2> { static constexpr int S = 5, G = 8, R = 2, DU = 1, T = 10; };
+template <> struct Pair<2> { static constexpr int S = 5, G = 8, R = 2, DU = 1, T = 10, KPS = 1; };
 static_assert(256 + Pair<2>::T * Cfg<2>::kSfColsPerStage <= kTmemCols, "MXFP4 scale slots");
 static_assert(256 + Pair<0>::T * Cfg<0>::kSfColsPerStage <= kTmemCols, "NVFP4 scale slots");
 static_assert(256 + Pair<1>::T * Cfg<1>::kSfColsPerStage <= kTmemCols, "MXFP8 scale slots");
 static_assert(Pair<0>::R >= Pair<0>::DU + 1 && Pair<1>::R >= Pair<1>::DU + 1, "scale ring depth");
+// a group never spans two tiles (whole scale units per tile) nor wraps the stage or slot rings;
+// grouped slots are released by sf_free, never by `empty` (which then counts groups)
+template <int kKind>
+constexpr bool pair_groups_ok() {
+    return Pair<kKind>::KPS == 1 ||
+           (Pair<kKind>::KPS == 2 && Pair<kKind>::G % 2 == 0 && Pair<kKind>::S % 2 == 0 && Pair<kKind>::T % 2 == 0 &&
+            Pair<kKind>::T != Pair<kKind>::S);
+}
+static_assert(pair_groups_ok<0>() && pair_groups_ok<1>() && pair_groups_ok<2>(), "K-block groups");
 constexpr uint32_t kHalfBBytes = 128 * kBKBytes;   // 16 KB
 constexpr uint32_t kPairStage = kABytes + kHalfBBytes;   // 32 KB, 1024-aligned
 template <int kKind>
@@ -1096,7 +1110,7 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
     constexpr int kEpiMode = PairOut<kOut>::kEpi;
     constexpr bool kTmaEpi = PairOut<kOut>::kTma;
     constexpr int S = Pair<kKind>::S, G = Pair<kKind>::G, R = Pair<kKind>::R, DU = Pair<kKind>::DU,
-                  T = Pair<kKind>::T;
+                  T = Pair<kKind>::T, KPS = Pair<kKind>::KPS, NB = S / KPS;
     constexpr uint32_t kSfCols = Cfg<kKind>::kSfColsPerStage;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1192,24 +1206,28 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         bool ok = true;
         int issued = 0;
         int64_t m0 = 0, n0 = 0, brow = 0;
-        for (int gk = 0, kb = 0, ti = 0; gk < total_kb && ok; ++gk) {
+        for (int gk = 0, kb = 0, ti = 0; gk < total_kb && ok; gk += KPS) {
             if (kb == 0) {
                 const int g = pair_tile(p, cid + ti * ncl, rank, m0, n0);
                 brow = (int64_t)g * p.N + n0 + 128 * rank;
             }
             while (ok && sf_u < total_units && sf_u <= gk / G + DU) ok = load_next_sf();
             if (!ok) break;
-            const int s = gk % S;
-            if (!mbar_wait_pair(&empty[s], ((uint32_t)(gk / S) & 1u) ^ 1u, wl)) break;
-            uint8_t* st = smem + s * kPairStage;
+            const int grp = gk / KPS, s = grp % NB;
+            if (!mbar_wait_pair(&empty[s], ((uint32_t)(grp / NB) & 1u) ^ 1u, wl)) break;
             if (lane == 0 && !p.no_copies) {
-                if (leader) mbar_arrive_expect_tx(&full[s], 2 * kPairStage);
+                if (leader) mbar_arrive_expect_tx(&full[s], KPS * 2 * kPairStage);
                 const uint32_t bar = leader_addr(&full[s]);
-                tma_load_2d_pair_hint(&p.tma_a, bar, st, kb * kBKBytes, (int32_t)m0, pol_a);
-                tma_load_2d_pair_hint(&p.tma_b, bar, st + kABytes, kb * kBKBytes, (int32_t)brow, pol_b);
+#pragma unroll
+                for (int j = 0; j < KPS; ++j) {
+                    uint8_t* st = smem + (s * KPS + j) * kPairStage;
+                    tma_load_2d_pair_hint(&p.tma_a, bar, st, (kb + j) * kBKBytes, (int32_t)m0, pol_a);
+                    tma_load_2d_pair_hint(&p.tma_b, bar, st + kABytes, (kb + j) * kBKBytes, (int32_t)brow, pol_b);
+                }
             }
-            issued = gk + 1;
-            if (++kb == p.num_kb) {
+            issued = grp + 1;
+            kb += KPS;
+            if (kb == p.num_kb) {
                 kb = 0;
                 ++ti;
             }
@@ -1220,8 +1238,8 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
         // (The failure-detection test mode issued none.)
         if (p.no_copies) issued = sf_u = 0;
         if (leader)
-            for (int gk = issued > S ? issued - S : 0; gk < issued; ++gk)
-                mbar_wait_pair(&full[gk % S], (uint32_t)(gk / S) & 1u, wl);
+            for (int grp = issued > NB ? issued - NB : 0; grp < issued; ++grp)
+                mbar_wait_pair(&full[grp % NB], (uint32_t)(grp / NB) & 1u, wl);
         for (int u = sf_u > R ? sf_u - R : 0; u < sf_u; ++u) mbar_wait(&sf_full[u % R], (uint32_t)(u / R) & 1u, wl);
     } else if (warp == 5) {
         // ------------------------------------------------ MMA issuer (leader only)
@@ -1233,14 +1251,15 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
                 tc_fence_after();
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     const int gk = ti * p.num_kb + kb;
-                    const int s = gk % S, t = gk % T;
-                    if (!mbar_wait_pair(&full[s], (uint32_t)(gk / S) & 1u, wl) ||
-                        !mbar_wait_pair(&sf_ready[t], (uint32_t)(gk / T) & 1u, wl)) {
+                    const int grp = gk / KPS, s = grp % NB, t = gk % T;
+                    const bool first = gk % KPS == 0;
+                    if ((first && !mbar_wait_pair(&full[s], (uint32_t)(grp / NB) & 1u, wl)) ||
+                        (first && !mbar_wait_pair(&sf_ready[t], (uint32_t)(gk / T) & 1u, wl))) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + s * kPairStage);
+                    if (first) tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (gk % S) * kPairStage);
                     const uint32_t sb = sa + kABytes;
                     const uint32_t sf_col = tmem + kSfCol + (uint32_t)t * kSfCols;
                     if (kKind == 0) {
@@ -1263,8 +1282,10 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
                                        kIdesc2Mxfp8 | ((uint32_t)j << 29) | ((uint32_t)j << 4),
                                        sf_col, sf_col + 4, (kb | j) ? 1u : 0u);
                     }
-                    tc_commit_pair(&empty[s]);
-                    if (T != S) tc_commit_pair(&sf_free[t]);   // T == S: the writers wait on `empty`
+                    if (gk % KPS == KPS - 1) {
+                        tc_commit_pair(&empty[s]);
+                        if (T != S) tc_commit_pair(&sf_free[t]);   // T == S: the writers wait on `empty`
+                    }
                 }
                 if (!ok) break;
                 // both CTAs' accumulators are complete once every MMA above has finished
@@ -1285,7 +1306,8 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
             // the staged unit's reads go out before the waits for the two tensor-memory slots
             PassScales<kKind> v;
             load_pass_scales<kKind>(sf_stage + r * kSfUnit, gk % G, p.b_sc_2d != 0, lane, warp, v);
-            if (!mbar_wait_pair(T == S ? &empty[t0] : &sf_free[t0], ((uint32_t)(gk / T) & 1u) ^ 1u, wl)) break;
+            if (KPS == 1 &&
+                !mbar_wait_pair(T == S ? &empty[t0] : &sf_free[t0], ((uint32_t)(gk / T) & 1u) ^ 1u, wl)) break;
             if (!mbar_wait_pair(T == S ? &empty[t1] : &sf_free[t1], ((uint32_t)((gk + 1) / T) & 1u) ^ 1u, wl)) break;
             tc_fence_after();
             store_pass_scales<kKind>(v, tmem + lane_base + kSfCol + (uint32_t)t0 * kSfCols,
@@ -1295,7 +1317,7 @@ gemm_pair_kernel(const __grid_constant__ Params p) {
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive_cluster(ready0 + (uint32_t)t0 * 8u);
-                mbar_arrive_cluster(ready0 + (uint32_t)t1 * 8u);
+                if (KPS == 1) mbar_arrive_cluster(ready0 + (uint32_t)t1 * 8u);
                 if ((gk + 1) % G == G - 1) mbar_arrive(&sf_empty[r]);
             }
         }
