@@ -195,6 +195,54 @@ class EventLog:
         return agg
 
 
+class StreamTap:
+    """Call hook of the end-to-end loop. Before a library call the compute stream waits for the
+    host-to-device copy of each step input whose memory one of the call's tensor arguments
+    overlaps (once per input); after the call an event marks its outputs ready, so that their
+    device-to-host copies start while the rest of the step runs. new_event() makes an event with
+    .record(stream); stream has .wait_event(event)."""
+
+    def __init__(self, new_event, stream, inputs, ready):
+        self.new_event, self.stream = new_event, stream
+        self.pending = [(t.data_ptr(), t.data_ptr() + t.numel() * t.element_size(), ev)
+                        for t, ev in zip(inputs, ready)]
+        self.done = {}
+
+    @staticmethod
+    def _tensors(args):
+        for a in args:
+            if isinstance(a, (tuple, list)):
+                yield from StreamTap._tensors(a)
+            elif hasattr(a, "data_ptr") and hasattr(a, "element_size"):
+                yield a
+
+    def wrap(self, kind, units, fn, *a, **k):
+        spans = [(t.data_ptr(), t.data_ptr() + t.numel() * t.element_size())
+                 for t in self._tensors(list(a) + list(k.values()))]
+        keep = []
+        for lo, hi, ev in self.pending:
+            if any(s0 < hi and lo < s1 for s0, s1 in spans):
+                self.stream.wait_event(ev)
+            else:
+                keep.append((lo, hi, ev))
+        self.pending = keep
+        out = fn(*a, **k)
+        ev = self.new_event()
+        ev.record(self.stream)
+        for t in self._tensors(out if isinstance(out, (tuple, list)) else [out]):
+            self.done[t.data_ptr()] = ev
+        return out
+
+    def finish(self):
+        """The step's remaining inputs (read by no call) are waited for all the same."""
+        for _, _, ev in self.pending:
+            self.stream.wait_event(ev)
+        self.pending = []
+
+    def ready(self, t):
+        return self.done.get(t.data_ptr())
+
+
 def mlp_step(F, torch, ins, log, seed, signs, outer="tensor"):
     """One forward + backward of the MLP block (layer.mlp_step), every call logged by kind.
     outer="row": the activations (X and GELU(H)) take one outer scale per token row and 4/6
@@ -583,33 +631,39 @@ def run_ours(args, rank, world, local_rank):
     d2h = 0
 
     def e2e_loop(nsteps):
+        # Each input has its own ready event and each call waits only for the inputs it reads
+        # (StreamTap), and each result is copied out once the call that makes it is done, so
+        # the first step starts after its first input's copy and the last step's earlier
+        # results leave while it runs.
         nonlocal outs_host, d2h
-        in_ready = [torch.cuda.Event() for _ in range(2)]
+        in_ready = [[torch.cuda.Event() for _ in host] for _ in range(2)]
         buf_free = [torch.cuda.Event() for _ in range(2)]
         out_done = torch.cuda.Event()
-        with torch.cuda.stream(copy):
-            for d, hsrc in zip(dbuf[0], host):
-                d.copy_(hsrc, non_blocking=True)
-            in_ready[0].record(copy)
+
+        def load(b):
+            with torch.cuda.stream(copy):
+                for d, hsrc, ev in zip(dbuf[b], host, in_ready[b]):
+                    d.copy_(hsrc, non_blocking=True)
+                    ev.record(copy)
+
+        load(0)
         for i in range(nsteps):
             b = i % 2
-            comp.wait_event(in_ready[b])
-            outs = mlp_step(F, torch, dbuf[b], log, seed, signs)
+            tap = StreamTap(torch.cuda.Event, comp, dbuf[b], in_ready[b])
+            outs = mlp_step(F, torch, dbuf[b], tap, seed, signs)
+            tap.finish()
             buf_free[b].record(comp)
             out_done.record(comp)
             if i + 1 < nsteps:
-                with torch.cuda.stream(copy):
-                    nb = (i + 1) % 2
-                    if i >= 1:
-                        copy.wait_event(buf_free[nb])
-                    for d, hsrc in zip(dbuf[nb], host):
-                        d.copy_(hsrc, non_blocking=True)
-                    in_ready[nb].record(copy)
+                nb = (i + 1) % 2
+                if i >= 1:
+                    copy.wait_event(buf_free[nb])
+                load(nb)
             with torch.cuda.stream(copy_out):
-                copy_out.wait_event(out_done)
                 if outs_host is None:
                     outs_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
                 for oh, o in zip(outs_host, outs):
+                    copy_out.wait_event(tap.ready(o) or out_done)
                     o.record_stream(copy_out)
                     oh.copy_(o, non_blocking=True)
             d2h = sum(o.numel() * o.element_size() for o in outs)

@@ -106,3 +106,45 @@ def test_step_config_names_the_workload():
     assert (c["tokens"], c["d_model"], c["ffn"]) == (16384, 4096, 16384)
     # six GEMMs of 2 M D F FLOPs each per step
     assert bench.STEP_FLOPS == 6 * 2.0 * 16384 * 4096 * 16384
+
+
+def test_stream_tap_waits_per_input_and_marks_outputs():
+    import torch
+
+    class Ev:
+        def __init__(self, name=""):
+            self.name, self.on = name, None
+
+        def record(self, stream):
+            self.on = stream
+
+    class Stream:
+        def __init__(self):
+            self.waits = []
+
+        def wait_event(self, ev):
+            self.waits.append(ev.name)
+
+    comp = Stream()
+    buf = torch.zeros(64, dtype=torch.bfloat16)
+    x, w1, w2, dy = buf[:16], buf[16:32], buf[32:48], buf[48:]
+    ready = [Ev(n) for n in ("x", "w1", "w2", "dy")]
+    made = []
+
+    def new_event():
+        made.append(Ev("call%d" % len(made)))
+        return made[-1]
+
+    tap = bench.StreamTap(new_event, comp, [x, w1, w2, dy], ready)
+    y = torch.zeros(4)
+    # a call on a view of x waits for x alone; a second use waits for nothing more
+    out = tap.wrap("k", 1, lambda t, s: (y, s), x[2:5], 3)
+    assert comp.waits == ["x"] and out[0] is y and tap.ready(y) is made[0] and made[0].on is comp
+    tap.wrap("k", 1, lambda t: None, x)
+    assert comp.waits == ["x"]
+    # nested arguments and keywords count; w1 and dy overlap, w2 does not
+    tap.wrap("k", 1, lambda *a, **k: None, [w1[:1], (3,)], amax_in=dy[-1:])
+    assert comp.waits == ["x", "w1", "dy"]
+    assert tap.ready(torch.zeros(1)) is None
+    tap.finish()
+    assert comp.waits == ["x", "w1", "dy", "w2"]
