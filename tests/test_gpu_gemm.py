@@ -247,6 +247,34 @@ def test_mxfp8_pair_kernel_structured_scales(F, orc):
     assert_bf16_rounding_of(got, orc.gemm_mxfp8(a, asc, b, bsc, with_abs=True), "MXFP8 pair structured, bf16 out")
 
 
+# Many short tiles per cluster (512 tiles of 256 x 256 over 76 CTA pairs, 4 K-blocks each): the
+# stage ring, the MXFP8 K-block groups and the tensor-memory scale slots wrap across tile
+# boundaries, and each tile's epilogue overlaps the next tile's main loop. Every output compared.
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_mxfp8_pair_kernel_many_short_tiles(F, orc, out_dtype):
+    M, N, K = 8192, 4096, 512
+    rng = np.random.default_rng(8192 + 512)
+    a, asc = rand_mxfp8(rng, M, K)
+    b, bsc = rand_mxfp8(rng, N, K)
+    d = run_mxfp8(F, a, asc, b, bsc, out_dtype)
+    ref = orc.gemm_mxfp8(a, asc, b, bsc, with_abs=True)
+    if out_dtype == torch.float32:
+        assert_gemm_close(d.cpu().numpy(), ref, f"MXFP8 pair {M}x{N}x{K}")
+    else:
+        assert_bf16_rounding_of(d.cpu().view(torch.int16).numpy().view(np.uint16), ref, f"MXFP8 pair {M}x{N}x{K} bf16")
+
+
+@pytest.mark.parametrize("two_d", [False, True])
+def test_nvfp4_pair_kernel_many_short_tiles(F, orc, two_d):
+    M, N, K = 8192, 4096, 1024
+    rng = np.random.default_rng(8192 + 1024 + two_d)
+    a, asc = rand_nvfp4(rng, M, K)
+    b, bsc = rand_nvfp4(rng, N, K, two_d)
+    d = run_nvfp4(F, a, asc, 0.5, b, bsc, 2 if two_d else 1, 0.125)
+    ref = orc.gemm_nvfp4(a, asc, 1, 0.5, b, bsc, 2 if two_d else 1, 0.125, with_abs=True)
+    assert_gemm_close(d.cpu().numpy(), ref, f"NVFP4 pair {M}x{N}x{K} 2d={two_d}")
+
+
 @pytest.mark.parametrize("M,N,K,two_d", [(300, 272, 8192, False), (256, 256, 8192, True)])
 def test_nvfp4_pair_kernel_random(F, orc, M, N, K, two_d):
     rng = np.random.default_rng(M * 3 + N + K)
